@@ -1,0 +1,434 @@
+"""Benchmark of the routed-expert cache hot path on one GB300 (or N replicas).
+
+Default workload: Qwen3.6-35B-A3B-shaped decode (40 MoE layers x 256 routed experts,
+top-8 + 1 shared expert, hidden 2048, intermediate 512, NVFP4 records in a pinned host
+pool, 600-slot global LRU cache, batch 1, locality p = 0.8, full offload q = m).
+A step is one decode token: all 40 layer calls (remap, load-through fills, gate/up,
+down + gated combine).  Inputs are resident in HBM; `e2e` repeats the run with the
+per-step inputs copied from pinned host memory and y copied back inside the timed
+region.  `--impl reference` times the CPU oracle on a bounded sample instead.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode tok/s & prefill tok/s; % of HBM/PCIe/FP4 roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=32)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen_decode")
+    ap.add_argument("--p", type=float, default=None, help="locality (default: the workload's)")
+    ap.add_argument("--split", default="full", choices=["full", "qstar"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled every 200 ms."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 6:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def record_parts(H, I):
+    gu = 2 * I * H // 2 + 2 * I * H // 16
+    d = H * I // 2 + H * I // 16
+    return gu, d
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def oracle_decode_sample(shape, seed, trace, gates, budget_s, max_calls=None):
+    """Time the CPU oracle (state + fp64 outputs) on a bounded sample of decode calls.
+    Returns (seconds per layer call, calls timed, description)."""
+    import numpy as np
+    import synth
+    from oracle.formats import decode_record, encode_record
+    from oracle.lru import SlotCache
+    from oracle.moe import RecordSource, decode_layer
+
+    s = shape
+    recs = {}
+
+    def rec(f):
+        if f not in recs:
+            recs[f] = encode_record(*[w.numpy() for w in synth.expert_weights(seed, f, s.H, s.I)])
+        return recs[f]
+
+    shared = {}
+    cache = SlotCache(s.L, s.E, s.C)
+    calls, spent = 0, 0.0
+    t_idx = 0
+    while spent < budget_s and (max_calls is None or calls < max_calls):
+        t, l = divmod(t_idx, s.L)
+        t_idx += 1
+        if t >= trace.shape[0]:
+            break
+        ids = trace[t, l]
+        for e in set(int(v) for v in ids.reshape(-1)):      # inputs: the pool records
+            rec(l * s.E + e)
+        if s.shared and l not in shared:
+            shared[l] = encode_record(*[w.numpy() for w in synth.shared_weights(seed, l, s.H, s.I)])
+        x = synth.decode_x(seed, t, l, s.L, s.B, s.H).float().numpy()
+        t0 = time.perf_counter()
+        cache.decode(l, ids)
+        src = RecordSource(rec, s.H, s.I)                    # fresh: decodes every expert
+        sh = decode_record(shared[l], s.H, s.I) if s.shared else None
+        decode_layer(x, ids, gates[t, l], l, s.E, src, sh)
+        spent += time.perf_counter() - t0
+        calls += 1
+    return spent / max(calls, 1), calls
+
+
+# ----------------------------------------------------------------- native decode bench
+
+def native_decode(args, rank, world):
+    import numpy as np
+    import torch
+    import expert_cache_gb300 as ft
+    from expert_cache_gb300.workloads import SHAPES, DecodeWorkload, build_pool, build_shared, split_tuple
+
+    s = SHAPES[args.workload]
+    if args.p is not None:
+        s.p = args.p
+    steps = args.warmup + args.steps
+    dev = torch.device("cuda")
+    pool = build_pool(args.seed, s.L, s.E, s.H, s.I)
+    shared = build_shared(args.seed, s.L, s.H, s.I) if s.shared else None
+    rec_bytes = ft.ft_record_bytes(s.H, s.I)
+
+    # B_P measured in this run (1 GiB pinned -> device, best of 5)
+    probe_n = min(1 << 30, pool.nbytes)
+    probe_dev = torch.empty(probe_n, dtype=torch.uint8, device=dev)
+    b_p = ft.ft_measure_h2d(pool.ptr, probe_dev, probe_n, 5)
+    del probe_dev
+    f_q16 = ft.ft_split_from_bandwidth(b_p, 2.0 * b_p)      # B_H = 2 B_P  ->  f = 1/2
+    split = split_tuple(args.split, f_q16)
+
+    wl = DecodeWorkload(s, seed=args.seed, steps=steps)
+    cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool.ptr, shared=shared, split=split)
+    stream = torch.cuda.current_stream()
+    hbm_gbs, _, peak_src = peaks()
+
+    def run(t0, t1):
+        for t in range(t0, t1):
+            wl.run_step(cache, t)
+
+    def timed(profile=False):
+        ft.ft_cache_resize(cache.handle, s.C, cache.slot_buf)   # empty cache, same trace
+        run(0, args.warmup)
+        if profile:
+            ft.ft_profile_enable(cache.handle, True)
+            ft.ft_profile_read(cache.handle)
+        torch.cuda.synchronize()
+        barrier(world)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run(args.warmup, steps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        prof = ft.ft_profile_read(cache.handle) if profile else None
+        if profile:
+            ft.ft_profile_enable(cache.handle, False)
+        return ev0.elapsed_time(ev1), prof
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms, _ = timed(False)
+    ms = max_over_ranks(ms, world)
+    _, prof = timed(True)
+
+    # algorithmic bytes from the per-call counters of the timed steps
+    ct = wl.counters[args.warmup:steps].cpu().numpy().astype(np.int64)   # [K, L, 4]
+    n_hit, n_fill = ct[..., 0].sum(), ct[..., 2].sum()
+    n_miss = ct[..., 1].sum()
+    n_shared = args.steps * s.L if s.shared else 0
+    gu_b, d_b = record_parts(s.H, s.I)
+    launches = args.steps * s.L
+    hbm_bytes_gu = (n_hit + n_shared) * gu_b
+    link_bytes = n_fill * rec_bytes
+    hbm_bytes_d = (n_hit + n_shared + n_fill) * d_b
+    t_gu_ms, n_gu = prof["gate_up"]
+    t_d_ms, n_d = prof["down"]
+    t_rm_ms, n_rm = prof["remap"]
+    # decode roofline: hit (+shared) records at HBM bandwidth + fills at B_P
+    t_roof_s = ((n_hit + n_shared) * rec_bytes / (hbm_gbs * 1e9) + link_bytes / (b_p * 1e9))
+    step_roof_ms = t_roof_s * 1e3 / args.steps
+    tok = args.steps * s.B * world
+    value = tok / (ms / 1e3)
+
+    per_launch_gu = (hbm_bytes_gu + link_bytes) / n_gu
+    t_gu_launch = t_gu_ms / 1e3 / n_gu
+    eff_peak_gu = (hbm_bytes_gu + link_bytes) / (hbm_bytes_gu / (hbm_gbs * 1e9) + link_bytes / (b_p * 1e9))
+    kernels = {
+        "remap": {"ms_total": t_rm_ms, "launches": n_rm},
+        "gate_up_fill": {"ms_total": t_gu_ms, "launches": n_gu},
+        "down_combine": {"ms_total": t_d_ms, "launches": n_d,
+                         "achieved_gbs": hbm_bytes_d / (t_d_ms / 1e3) / 1e9 if t_d_ms else None},
+    }
+    roofline = {
+        "kernel": "gate_up_kernel (hits from HBM, fills load-through from pinned host)",
+        "bound": "hbm",
+        "achieved": per_launch_gu / t_gu_launch / 1e9,
+        "peak": eff_peak_gu / 1e9,
+        "unit": "GB/s",
+        "frac": (per_launch_gu / t_gu_launch) / eff_peak_gu,
+        "traffic": None,
+        "peak_note": (f"byte-mix peak of this kernel: HBM bytes at {hbm_gbs:.0f} GB/s ({peak_src} "
+                      f"MEASURED_PEAKS hbm_gbs) plus host-link bytes at B_P = {b_p:.1f} GB/s "
+                      "measured in this run"),
+        "hbm_bytes_per_launch": hbm_bytes_gu / n_gu,
+        "link_bytes_per_launch": link_bytes / n_gu,
+    }
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 weights x bf16 activations, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": s.name, "L": s.L, "E": s.E, "top_k": s.k, "shared_expert": s.shared,
+                   "H": s.H, "I": s.I, "capacity": s.C, "B": s.B, "locality_p": s.p,
+                   "split": args.split, "f_q16": split[1], "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (slot cache %.2f GB, host pool %.1f GB)"
+                         % (s.C * rec_bytes / 1e9, s.L * s.E * rec_bytes / 1e9)},
+        "decode_roofline": {"ms_per_step_roofline": step_roof_ms,
+                            "frac": step_roof_ms / (ms / args.steps),
+                            "b_p_gbs": b_p, "hbm_gbs": hbm_gbs, "hbm_source": peak_src,
+                            "hits_per_step": n_hit / args.steps, "misses_per_step": n_miss / args.steps,
+                            "fills_per_step": n_fill / args.steps,
+                            "miss_rate": float(n_miss / max(n_hit + n_miss, 1))},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": 3 * launches,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        out["e2e"] = native_e2e(args, s, wl, cache, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, calls = oracle_decode_sample(s, args.seed, wl.trace, wl.gates, budget_s=20.0)
+        out["cpu_baseline"] = {"value": 1.0 / (sec * s.L) * s.B, "unit": "tok/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"{calls} decode layer calls of this workload (state "
+                                         f"oracle + fp64 outputs), extrapolated to {s.L} layers"}
+    cache.close()
+    pool.free()
+    return out
+
+
+def native_e2e(args, s, wl, cache, stream, world):
+    """Same steps through the C ABI with the step's inputs in pinned host memory:
+    H2D of x/ids/gates and D2H of y inside the timed region."""
+    import torch
+    import expert_cache_gb300 as ft
+    steps = args.warmup + args.steps
+    hx = wl.x.cpu().pin_memory()
+    hid = wl.ids.cpu().pin_memory()
+    hw = wl.w.cpu().pin_memory()
+    hy = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
+    dx = torch.empty_like(wl.x[0])
+    di = torch.empty_like(wl.ids[0])
+    dw = torch.empty_like(wl.w[0])
+    dy = torch.empty_like(wl.y[0])
+    dd = torch.empty_like(wl.deferred[0])
+
+    def step(t):
+        dx.copy_(hx[t], non_blocking=True)
+        di.copy_(hid[t], non_blocking=True)
+        dw.copy_(hw[t], non_blocking=True)
+        for l in range(s.L):
+            ft.ft_moe_decode(cache.handle, l, dx[l], di[l], dw[l], s.B, s.k, dy[l], dd[l], None, None)
+        hy[t].copy_(dy, non_blocking=True)
+
+    ft.ft_cache_resize(cache.handle, s.C, cache.slot_buf)
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for t in range(args.warmup, steps):
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    h2d = dx.numel() * dx.element_size() + di.numel() * 4 + dw.numel() * 4
+    d2h = dy.numel() * 4
+    return {"value": args.steps * s.B * world / (ms / 1e3), "unit": "tok/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def reference(args, rank, world):
+    """The CPU oracle, as it stands, timed on the host cores: each step is a bounded
+    sample (one decode layer call of the workload), extrapolated to a whole token."""
+    import synth
+    from expert_cache_gb300.workloads import SHAPES
+    s = SHAPES[args.workload]
+    if args.p is not None:
+        s.p = args.p
+    k_steps = args.warmup + args.steps
+    trace = synth.locality_trace(args.seed, s.L, s.E, s.k, s.B, (k_steps + s.L - 1) // s.L + 1, s.p)
+    gates = synth.decode_gates(args.seed, trace.shape[0], s.L, s.B, s.k)
+    budget = 240.0
+    t0 = time.perf_counter()
+    sec, calls = oracle_decode_sample(s, args.seed, trace, gates, budget_s=budget,
+                                      max_calls=args.steps)
+    wall = time.perf_counter() - t0
+    value = s.B / (sec * s.L)
+    return {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": calls, "warmup": 0, "ms_per_step": sec * s.L * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": s.name, "L": s.L, "E": s.E, "top_k": s.k, "H": s.H, "I": s.I,
+                       "capacity": s.C, "B": s.B, "locality_p": s.p, "split": "full"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{calls} decode layer calls (state oracle + fp64 outputs), "
+                                       f"each extrapolated to {s.L} layers; wall {wall:.0f} s"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        print(json.dumps(reference(args, rank, world)), flush=True)
+        return
+    rank, world = dist_setup(args)
+    out = native_decode(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

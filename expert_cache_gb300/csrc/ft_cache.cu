@@ -1,0 +1,451 @@
+// Host side of the C ABI: cache creation over caller-owned memory, the decode
+// call sequence, resize at a safe point, snapshots, the split helpers, pinned
+// memory, the H2D probe and per-kernel profiling.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "ft_internal.cuh"
+
+namespace ft {
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+WsLayout ws_layout(const ft_cache_desc& d) {
+    WsLayout w{};
+    const int cmax = d.capacity_max > 0 ? d.capacity_max : d.capacity;
+    const size_t R = (size_t)d.B_max * d.k_max;
+    const size_t P = R + d.B_max;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.slot_for_id = take((size_t)d.L * d.E * 4);
+    w.id_of_slot = take((size_t)cmax * 4);
+    w.usage = take((size_t)cmax * 8);
+    w.lru_order = take((size_t)cmax * 4);
+    w.scalars = take(sizeof(DevScalars));
+    w.units = take((R + 1) * sizeof(Unit));
+    w.route_pair = take(R * 4);
+    w.pair_tok = take(P * 4);
+    w.h = take(P * (size_t)d.I * 4);
+    w.o = take(P * (size_t)d.H * 4);
+    w.tile_done = take((size_t)(d.H / kDownRowsPerItem + 1) * 4);
+    w.prefill = off;
+    w.prefill_bytes = 0;
+    w.total = off;
+    return w;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+}  // namespace ft
+
+using namespace ft;
+
+static const char* kStatusNames[] = {"ok", "bad argument", "CUDA error", "not enough capacity",
+                                     "bad state", "device wait timed out", "host pool not pinned"};
+
+static ft_status fail(ft_cache* c, ft_status s, const char* msg) {
+    if (c) snprintf(c->err, sizeof(c->err), "%s", msg);
+    return s;
+}
+
+static ft_status cuda_fail(ft_cache* c, cudaError_t e, const char* where) {
+    if (c) snprintf(c->err, sizeof(c->err), "%s: %s", where, cudaGetErrorString(e));
+    return FT_ERR_CUDA;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static ft_status check_desc(const ft_cache_desc* d) {
+    if (!d) return FT_ERR_ARG;
+    const int cmax = d->capacity_max > 0 ? d->capacity_max : d->capacity;
+    if (d->L < 1 || d->E < 1 || d->E > kMaxE) return FT_ERR_ARG;
+    if (d->H < 64 || d->H % 64 || d->H > 65536) return FT_ERR_ARG;
+    if (d->I < 32 || d->I % 32 || d->I > 65536) return FT_ERR_ARG;
+    if (d->k_max < 1 || d->k_max > kMaxK || d->B_max < 1 || d->B_max > kMaxB) return FT_ERR_ARG;
+    if (d->B_max * d->k_max > kMaxRoutes) return FT_ERR_ARG;
+    if (d->capacity < 1 || d->capacity > kMaxC || cmax < d->capacity || cmax > kMaxC) return FT_ERR_ARG;
+    if ((long long)d->L * d->E > (1LL << 30) || d->T_max < 0) return FT_ERR_ARG;
+    if (d->split.mode != FT_SPLIT_FULL_OFFLOAD && d->split.mode != FT_SPLIT_QSTAR) return FT_ERR_ARG;
+    if (d->split.mode == FT_SPLIT_QSTAR && (d->split.f_q16 < 1 || d->split.f_q16 > 65536)) return FT_ERR_ARG;
+    return FT_OK;
+}
+
+extern "C" {
+
+ft_status ft_record_bytes(int32_t H, int32_t I, size_t* bytes) {
+    if (!bytes || H < 64 || H % 64 || I < 32 || I % 32) return FT_ERR_ARG;
+    *bytes = record_layout(H, I).bytes;
+    return FT_OK;
+}
+
+ft_status ft_cache_required_sizes(const ft_cache_desc* d, size_t* record_bytes,
+                                  size_t* workspace_bytes) {
+    ft_status s = check_desc(d);
+    if (s != FT_OK) return s;
+    if (record_bytes) *record_bytes = record_layout(d->H, d->I).bytes;
+    if (workspace_bytes) *workspace_bytes = ws_layout(*d).total;
+    return FT_OK;
+}
+
+ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
+    if (!out) return FT_ERR_ARG;
+    *out = nullptr;
+    ft_status s = check_desc(d);
+    if (s != FT_OK) return s;
+    if (!d->host_pool || !d->slot_buf || !d->workspace) return FT_ERR_ARG;
+    if (!aligned(d->slot_buf, 256) || !aligned(d->workspace, 256) || !aligned(d->host_pool, 256))
+        return FT_ERR_ARG;
+    if (d->shared_experts && !aligned(d->shared_experts, 256)) return FT_ERR_ARG;
+
+    cudaPointerAttributes pa;
+    cudaError_t e = cudaPointerGetAttributes(&pa, d->host_pool);
+    if (e != cudaSuccess || pa.type != cudaMemoryTypeHost || !pa.devicePointer) {
+        cudaGetLastError();
+        return FT_ERR_UNPINNED;
+    }
+    cudaPointerAttributes pw, psb;
+    if (cudaPointerGetAttributes(&pw, d->workspace) != cudaSuccess ||
+        cudaPointerGetAttributes(&psb, d->slot_buf) != cudaSuccess ||
+        (pw.type != cudaMemoryTypeDevice && pw.type != cudaMemoryTypeManaged) ||
+        (psb.type != cudaMemoryTypeDevice && psb.type != cudaMemoryTypeManaged)) {
+        cudaGetLastError();
+        return FT_ERR_ARG;
+    }
+
+    ft_cache* c = new (std::nothrow) ft_cache();
+    if (!c) return FT_ERR_ARG;
+    c->d = *d;
+    if (c->d.capacity_max <= 0) c->d.capacity_max = d->capacity;
+    c->rec = record_layout(d->H, d->I);
+    c->ws = ws_layout(c->d);
+    c->C = d->capacity;
+    c->host_pool_dev = static_cast<const uint8_t*>(pa.devicePointer);
+    c->slot_buf = static_cast<uint8_t*>(d->slot_buf);
+    c->workspace = static_cast<uint8_t*>(d->workspace);
+    c->buffer_layer[0] = c->buffer_layer[1] = -1;
+    c->copy_pending = false;
+    c->prof = false;
+    c->prof_n = 0;
+    c->err[0] = 0;
+    c->grid_gemv = sm_count() * gemv_occupancy(d->H, d->I);
+
+    if ((e = cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking)) != cudaSuccess) {
+        delete c;
+        return FT_ERR_CUDA;
+    }
+    for (int i = 0; i < 2; ++i) {
+        cudaEventCreateWithFlags(&c->copy_done[i], cudaEventDisableTiming);
+        cudaEventCreateWithFlags(&c->compute_done[i], cudaEventDisableTiming);
+    }
+    uint8_t* ws = c->workspace;
+    e = launch_init_tables(reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id), d->L * d->E,
+                           reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot),
+                           reinterpret_cast<long long*>(ws + c->ws.usage),
+                           reinterpret_cast<int32_t*>(ws + c->ws.lru_order), c->C,
+                           reinterpret_cast<DevScalars*>(ws + c->ws.scalars), true, c->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->copy_stream);
+    if (e != cudaSuccess) {
+        ft_cache_destroy(c);
+        return FT_ERR_CUDA;
+    }
+    *out = c;
+    return FT_OK;
+}
+
+void ft_cache_destroy(ft_cache* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->copy_stream);
+    for (int i = 0; i < 2; ++i) {
+        cudaEventDestroy(c->copy_done[i]);
+        cudaEventDestroy(c->compute_done[i]);
+    }
+    if (c->prof_n >= 0) {
+        for (int i = 0; i < ft_cache::kProfEvents; ++i)
+            if (c->prof_ev[i]) cudaEventDestroy(c->prof_ev[i]);
+    }
+    cudaStreamDestroy(c->copy_stream);
+    delete c;
+}
+
+ft_status ft_cache_capacity(const ft_cache* c, int32_t* capacity) {
+    if (!c || !capacity) return FT_ERR_ARG;
+    *capacity = c->C;
+    return FT_OK;
+}
+
+ft_status ft_set_split(ft_cache* c, ft_split s) {
+    if (!c) return FT_ERR_ARG;
+    if (s.mode != FT_SPLIT_FULL_OFFLOAD && s.mode != FT_SPLIT_QSTAR)
+        return fail(c, FT_ERR_ARG, "split mode");
+    if (s.mode == FT_SPLIT_QSTAR && (s.f_q16 < 1 || s.f_q16 > 65536))
+        return fail(c, FT_ERR_ARG, "f_q16 outside [1, 65536]");
+    c->d.split = s;
+    return FT_OK;
+}
+
+static uint32_t frac_q16(double f) {
+    if (!(f > 0)) return 0;
+    if (f > 1) f = 1;
+    double q = std::floor(f * 65536.0 + 0.5);
+    return q > 65536.0 ? 65536u : (uint32_t)q;
+}
+
+uint32_t ft_split_from_bandwidth(double B_P, double B_H) {
+    if (!(B_P > 0) || !(B_H > 0)) return 0;
+    return frac_q16(B_P / B_H);
+}
+
+uint32_t ft_split_from_overlap(double p_ov, double c_ov) {
+    if (!(p_ov > 0) || !(c_ov >= 0)) return 0;
+    return frac_q16(p_ov / (p_ov + c_ov));
+}
+
+// ------------------------------------------------------------------ profiling
+
+static void prof_fold(ft_cache* c) {
+    if (c->prof_n == 0) return;
+    cudaEventSynchronize(c->prof_ev[2 * c->prof_n - 1]);
+    for (int i = 0; i < c->prof_n; ++i) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]) == cudaSuccess) {
+            c->prof_ms[c->prof_kind[i]] += ms;
+            c->prof_launches[c->prof_kind[i]] += 1;
+        }
+    }
+    c->prof_n = 0;
+}
+
+// Records the "before" event of a launch of `kind`; returns the pair index or -1.
+static int prof_begin(ft_cache* c, int kind, cudaStream_t s) {
+    if (!c->prof) return -1;
+    if (c->prof_n * 2 + 2 > ft_cache::kProfEvents) prof_fold(c);
+    const int i = c->prof_n++;
+    c->prof_kind[i] = kind;
+    cudaEventRecord(c->prof_ev[2 * i], s);
+    return i;
+}
+
+static void prof_end(ft_cache* c, int i, cudaStream_t s) {
+    if (i >= 0) cudaEventRecord(c->prof_ev[2 * i + 1], s);
+}
+
+ft_status ft_profile_enable(ft_cache* c, int32_t enable) {
+    if (!c) return FT_ERR_ARG;
+    if (enable && !c->prof_ev[0]) {
+        for (int i = 0; i < ft_cache::kProfEvents; ++i)
+            if (cudaEventCreate(&c->prof_ev[i]) != cudaSuccess) return FT_ERR_CUDA;
+    }
+    if (!enable) prof_fold(c);
+    c->prof = enable != 0;
+    return FT_OK;
+}
+
+ft_status ft_profile_read(ft_cache* c, double* total_ms, int64_t* launches) {
+    if (!c) return FT_ERR_ARG;
+    prof_fold(c);
+    for (int k = 0; k < FT_PROF_KINDS; ++k) {
+        if (total_ms) total_ms[k] = c->prof_ms[k];
+        if (launches) launches[k] = c->prof_launches[k];
+        c->prof_ms[k] = 0;
+        c->prof_launches[k] = 0;
+    }
+    return FT_OK;
+}
+
+// ------------------------------------------------------------------ decode
+
+ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t* topk_ids,
+                        const float* topk_w, int32_t B, int32_t k, float* y,
+                        int32_t* deferred, int32_t* route_slot, int32_t* counters,
+                        void* stream) {
+    if (!c) return FT_ERR_ARG;
+    if (layer < 0 || layer >= c->d.L) return fail(c, FT_ERR_ARG, "layer out of range");
+    if (B < 1 || B > c->d.B_max) return fail(c, FT_ERR_ARG, "B outside [1, B_max]");
+    if (k < 1 || k > c->d.k_max) return fail(c, FT_ERR_ARG, "k outside [1, k_max]");
+    if (!x || !topk_ids || !topk_w || !y || !deferred) return fail(c, FT_ERR_ARG, "NULL argument");
+    if (!aligned(x, 16)) return fail(c, FT_ERR_ARG, "x must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (c->copy_pending) {   // a prefill stream-in may still be writing slots
+        cudaStreamWaitEvent(s, c->copy_done[0], 0);
+        cudaStreamWaitEvent(s, c->copy_done[1], 0);
+        c->copy_pending = false;
+    }
+    c->buffer_layer[0] = c->buffer_layer[1] = -1;   // decode may evict prefill buffers
+
+    uint8_t* ws = c->workspace;
+    DecodeArgs a;
+    a.slot_for_id = reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id);
+    a.id_of_slot = reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot);
+    a.usage = reinterpret_cast<long long*>(ws + c->ws.usage);
+    a.lru_order = reinterpret_cast<int32_t*>(ws + c->ws.lru_order);
+    a.sc = reinterpret_cast<DevScalars*>(ws + c->ws.scalars);
+    a.units = reinterpret_cast<Unit*>(ws + c->ws.units);
+    a.route_pair = reinterpret_cast<int32_t*>(ws + c->ws.route_pair);
+    a.pair_tok = reinterpret_cast<int32_t*>(ws + c->ws.pair_tok);
+    a.h = reinterpret_cast<float*>(ws + c->ws.h);
+    a.o = reinterpret_cast<float*>(ws + c->ws.o);
+    a.tile_done = reinterpret_cast<unsigned*>(ws + c->ws.tile_done);
+    a.host_pool = c->host_pool_dev;
+    a.slot_buf = c->slot_buf;
+    a.shared = static_cast<const uint8_t*>(c->d.shared_experts);
+    a.rec_bytes = c->rec.bytes;
+    a.off_gu_scales = c->rec.gu_scales;
+    a.off_d_codes = c->rec.d_codes;
+    a.off_d_scales = c->rec.d_scales;
+    a.off_s_gu = c->rec.s_gu;
+    a.off_s_d = c->rec.s_d;
+    a.L = c->d.L; a.E = c->d.E; a.H = c->d.H; a.I = c->d.I; a.C = c->C;
+    a.layer = layer; a.B = B; a.k = k;
+    a.split_mode = c->d.split.mode;
+    a.f_q16 = c->d.split.f_q16;
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.ids = topk_ids;
+    a.w = topk_w;
+    a.y = y;
+    a.deferred = deferred;
+    a.route_slot = route_slot;
+    a.counters = counters;
+
+    cudaError_t e;
+    int p = prof_begin(c, 0, s);
+    e = launch_remap(a, s);
+    prof_end(c, p, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "remap launch");
+    p = prof_begin(c, 1, s);
+    e = launch_gate_up(a, c->grid_gemv, s);
+    prof_end(c, p, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "gate/up launch");
+    p = prof_begin(c, 2, s);
+    e = launch_down(a, c->grid_gemv, s);
+    prof_end(c, p, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "down launch");
+    return FT_OK;
+}
+
+// ------------------------------------------------------------------ resize / state
+
+ft_status ft_cache_resize(ft_cache* c, int32_t new_capacity, void* new_slot_buf, void* stream) {
+    if (!c) return FT_ERR_ARG;
+    if (new_capacity < 1 || new_capacity > c->d.capacity_max)
+        return fail(c, FT_ERR_ARG, "new_capacity outside [1, capacity_max]");
+    if (!new_slot_buf || !aligned(new_slot_buf, 256)) return fail(c, FT_ERR_ARG, "slot buffer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cuda_fail(c, cudaGetLastError(), "capture query");
+    if (cs != cudaStreamCaptureStatusNone) return fail(c, FT_ERR_STATE, "resize while capturing");
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->copy_stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "resize drain");
+    c->C = new_capacity;
+    c->slot_buf = static_cast<uint8_t*>(new_slot_buf);
+    c->buffer_layer[0] = c->buffer_layer[1] = -1;
+    c->copy_pending = false;
+    uint8_t* ws = c->workspace;
+    e = launch_init_tables(reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id), c->d.L * c->d.E,
+                           reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot),
+                           reinterpret_cast<long long*>(ws + c->ws.usage),
+                           reinterpret_cast<int32_t*>(ws + c->ws.lru_order), c->C,
+                           reinterpret_cast<DevScalars*>(ws + c->ws.scalars), false, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "resize rebuild");
+    return FT_OK;
+}
+
+ft_status ft_cache_snapshot(ft_cache* c, int32_t* slot_for_id, int32_t* id_of_slot,
+                            int64_t* usage, int64_t* tick) {
+    if (!c) return FT_ERR_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    const uint8_t* ws = c->workspace;
+    if (e == cudaSuccess && slot_for_id)
+        e = cudaMemcpy(slot_for_id, ws + c->ws.slot_for_id, (size_t)c->d.L * c->d.E * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && id_of_slot)
+        e = cudaMemcpy(id_of_slot, ws + c->ws.id_of_slot, (size_t)c->C * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && usage)
+        e = cudaMemcpy(usage, ws + c->ws.usage, (size_t)c->C * 8, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && tick)
+        e = cudaMemcpy(tick, ws + c->ws.scalars + offsetof(DevScalars, tick), 8, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? FT_OK : cuda_fail(c, e, "snapshot");
+}
+
+ft_status ft_cache_status(ft_cache* c, int32_t* device_status) {
+    if (!c || !device_status) return FT_ERR_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    int* st = reinterpret_cast<int*>(c->workspace + c->ws.scalars + offsetof(DevScalars, status));
+    if (e == cudaSuccess) e = cudaMemcpy(device_status, st, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(st, 0, 4);
+    return e == cudaSuccess ? FT_OK : cuda_fail(c, e, "status");
+}
+
+// ------------------------------------------------------------------ utilities
+
+ft_status ft_quantize_experts(const float* w_gu, const float* w_d, int32_t n, int32_t H,
+                              int32_t I, void* records, void* stream) {
+    if (!w_gu || !w_d || !records || n < 1 || H < 64 || H % 64 || I < 32 || I % 32) return FT_ERR_ARG;
+    if (!aligned(w_gu, 16) || !aligned(w_d, 16) || !aligned(records, 256)) return FT_ERR_ARG;
+    cudaError_t e = launch_quantize(w_gu, w_d, n, H, I, static_cast<uint8_t*>(records),
+                                    record_layout(H, I).bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_pinned_alloc(size_t bytes, void** out) {
+    if (!out || !bytes) return FT_ERR_ARG;
+    *out = nullptr;
+    cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return FT_ERR_CUDA;
+    }
+    return FT_OK;
+}
+
+ft_status ft_pinned_free(void* p) {
+    if (!p) return FT_ERR_ARG;
+    return cudaFreeHost(p) == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t reps, double* gbps) {
+    if (!pinned || !dev || !bytes || reps < 1 || !gbps) return FT_ERR_ARG;
+    cudaStream_t s;
+    cudaEvent_t a, b;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return FT_ERR_CUDA;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    float best = 0.f;
+    cudaError_t e = cudaSuccess;
+    for (int r = 0; r <= reps && e == cudaSuccess; ++r) {   // first copy is a warm-up
+        cudaEventRecord(a, s);
+        e = cudaMemcpyAsync(dev, pinned, bytes, cudaMemcpyHostToDevice, s);
+        cudaEventRecord(b, s);
+        if (e == cudaSuccess) e = cudaEventSynchronize(b);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, a, b);
+        if (r > 0 && (best == 0.f || ms < best)) best = ms;
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    cudaStreamDestroy(s);
+    if (e != cudaSuccess || best <= 0.f) return FT_ERR_CUDA;
+    *gbps = (double)bytes / (best * 1e-3) / 1e9;
+    return FT_OK;
+}
+
+const char* ft_status_string(ft_status s) {
+    if (s < 0 || s > 6) return "unknown status";
+    return kStatusNames[s];
+}
+
+const char* ft_last_error(const ft_cache* c) { return c ? c->err : ""; }
+
+}  // extern "C"

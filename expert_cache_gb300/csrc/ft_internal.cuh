@@ -1,0 +1,188 @@
+// Internal declarations of the expert-cache library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/ft.h"
+
+namespace ft {
+
+// ----------------------------------------------------------------- limits
+constexpr int kThreadsRemap = 1024;
+constexpr int kMaxE = 4096;            // experts per layer
+constexpr int kMaxC = 16384;           // slots
+constexpr int kMaxRoutes = 1023;       // B_max * k_max
+constexpr int kMaxB = 32;
+constexpr int kMaxK = 32;
+constexpr int kSlotsPerThread = kMaxC / kThreadsRemap;     // 16
+constexpr int kExpertsPerThread = kMaxE / kThreadsRemap;   // 4
+
+// Expert GEMV tiling.
+constexpr int kGemvThreads = 256;      // 8 warps
+constexpr int kRowPairsPerItem = 16;   // gate/up row pairs per gate-up work item
+constexpr int kDownRowsPerItem = 64;   // output rows per down work item
+constexpr int kTokGroup = 4;           // tokens accumulated per pass
+constexpr int kCopyChunk = 32768;      // bytes per W_d copy work item of a fill
+
+// ----------------------------------------------------------------- record
+struct RecordLayout {
+    size_t gu_codes, gu_scales, d_codes, d_scales, s_gu, s_d;
+    size_t raw, bytes;
+};
+
+inline RecordLayout record_layout(int H, int I) {
+    RecordLayout r;
+    size_t off = 0;
+    r.gu_codes = off;  off += (size_t)2 * I * H / 2;
+    r.gu_scales = off; off += (size_t)2 * I * H / 16;
+    r.d_codes = off;   off += (size_t)H * I / 2;
+    r.d_scales = off;  off += (size_t)H * I / 16;
+    r.s_gu = off;      off += 4;
+    r.s_d = off;       off += 4;
+    r.raw = off;
+    r.bytes = (off + 255) / 256 * 256;
+    return r;
+}
+
+// ----------------------------------------------------------------- device state
+// Scalars kept in the workspace (device).
+struct DevScalars {
+    long long tick;        // one tick per decode / prefill layer call
+    int status;            // FT_DEV_* bits
+    int n_units;           // GPU units of the current decode call (fills, hits, shared)
+    int n_fill;            // q
+    int n_hit;
+    int n_pairs;           // (unit, token) pairs
+    int shared_pair0;      // first pair of the shared unit, or -1
+    unsigned work1;        // gate/up work counter
+    unsigned work2;        // down work counter
+    int counters[4];       // n_hit, m, q, deferred routes
+    int pad[2];
+};
+
+// One expert computed on the GPU in a decode call.
+struct Unit {
+    const uint8_t* src;    // record to read: slot (hit), host pool (fill), shared
+    uint8_t* dst;          // slot to write while reading (fill), else nullptr
+    int pair0;             // first (unit, token) pair
+    int n_tok;             // number of tokens routed to this unit
+};
+
+// Offsets of the workspace regions (bytes, 256-aligned).
+struct WsLayout {
+    size_t slot_for_id, id_of_slot, usage, lru_order, scalars;
+    size_t units, route_pair, pair_tok, h, o, tile_done;
+    size_t prefill;        // start of the prefill region (0 bytes if T_max == 0)
+    size_t prefill_bytes;
+    size_t total;
+};
+
+WsLayout ws_layout(const ft_cache_desc& d);
+
+// Arguments of one decode call, passed by value to every decode kernel.
+struct DecodeArgs {
+    int32_t* slot_for_id;
+    int32_t* id_of_slot;
+    long long* usage;
+    int32_t* lru_order;
+    DevScalars* sc;
+    Unit* units;
+    int32_t* route_pair;
+    int32_t* pair_tok;
+    float* h;              // [n_pairs, I]
+    float* o;              // [n_pairs, H]
+    unsigned* tile_done;   // [H / kDownRowsPerItem]
+    const uint8_t* host_pool;   // device-mapped address of the pinned pool
+    uint8_t* slot_buf;
+    const uint8_t* shared;      // device, or nullptr
+    size_t rec_bytes;
+    size_t off_gu_scales, off_d_codes, off_d_scales, off_s_gu, off_s_d;
+    int L, E, H, I, C, layer, B, k;
+    int split_mode;
+    unsigned f_q16;
+    const __nv_bfloat16* x;
+    const int32_t* ids;
+    const float* w;
+    float* y;
+    int32_t* deferred;
+    int32_t* route_slot;
+    int32_t* counters;
+};
+
+// Kernel launchers (each returns the launch error).
+cudaError_t launch_init_tables(int32_t* slot_for_id, int n_ids, int32_t* id_of_slot,
+                               long long* usage, int32_t* lru_order, int C,
+                               DevScalars* sc, bool reset_tick, cudaStream_t s);
+cudaError_t launch_remap(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_gate_up(const DecodeArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down(const DecodeArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
+                            uint8_t* records, size_t rec_bytes, cudaStream_t s);
+
+int sm_count();
+int gemv_occupancy(int H, int I);
+
+// ----------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+
+// Exclusive prefix sum over the whole block (blockDim.x a multiple of 32, <= 1024).
+// All threads must call it.  `buf` is 33 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* buf) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) buf[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int s = lane < nw ? buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += t;
+        }
+        buf[lane] = s;
+    }
+    __syncthreads();
+    const int base = wid ? buf[wid - 1] : 0;
+    if (total) *total = buf[nw - 1];
+    __syncthreads();
+    return base + incl - v;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace ft
+
+struct ft_cache {
+    ft_cache_desc d;
+    ft::RecordLayout rec;
+    ft::WsLayout ws;
+    int C;                          // current slot count
+    const uint8_t* host_pool_dev;   // device-mapped pool address
+    uint8_t* slot_buf;
+    uint8_t* workspace;
+    cudaStream_t copy_stream;
+    cudaEvent_t copy_done[2];       // prefill buffer loaded
+    cudaEvent_t compute_done[2];    // prefill buffer no longer read
+    int buffer_layer[2];            // layer last streamed into each prefill buffer (-1 none)
+    bool copy_pending;
+    int grid_gemv;
+    // profiling
+    bool prof;
+    static constexpr int kProfEvents = 65536;
+    cudaEvent_t prof_ev[kProfEvents];
+    int prof_kind[kProfEvents / 2];
+    int prof_n;
+    double prof_ms[FT_PROF_KINDS];
+    long long prof_launches[FT_PROF_KINDS];
+    char err[256];
+};

@@ -1,0 +1,261 @@
+// Prefill helper kernels: slot tables of the full-layer buffers, stable route sort
+// by expert, NVFP4 activation quantisation into sorted row order, and the combine.
+//
+// [EXPLAINER §4.2-4.3] two whole-layer buffers borrowed from the global slot pool;
+// what they hold afterwards is decode's initial cache.  [EXPLAINER §1.1] the MoE
+// output y[t] = sum_j p_{t,j} Expert_{l,e_{t,j}}(x_t).  The activation quantiser
+// (unit tensor scale, E4M3 per 16, E2M1 codes) runs in fp32 IEEE steps.
+#include "ft_prefill.cuh"
+#include "ft_quant.cuh"
+
+namespace ft {
+
+// ------------------------------------------------------------------ slot tables
+// One CTA of 1024 threads.  Maps layer `la` into buffer ba (and, if lb >= 0, layer
+// lb into buffer bb), with the same outcome as loading expert by expert: each
+// buffer slot b*E + e ends up holding flat id l*E + e; an id evicted from a buffer
+// slot is unmapped; a slot outside the buffers that held an expert of the loaded
+// layer becomes free.  Then every buffer slot is stamped with the call's tick and
+// the LRU order is rebuilt: free slots ascending, untouched occupied slots in their
+// old order, then the touched slots ascending.
+__global__ void __launch_bounds__(1024, 1) pf_tables_kernel(PrefillTablesArgs a) {
+    __shared__ int s_scan[33];
+    __shared__ long long s_tick;
+    const int tid = threadIdx.x;
+    const int C = a.C, E = a.E;
+    if (tid == 0) {
+        s_tick = a.sc->tick + 1;
+        a.sc->tick = s_tick;
+    }
+    __syncthreads();
+    for (int pass = 0; pass < 2; ++pass) {
+        const int l = pass == 0 ? a.la : a.lb;
+        const int b = pass == 0 ? a.ba : a.bb;
+        if (l < 0) break;
+        for (int s = tid; s < C; s += 1024) {
+            const int f_old = a.id_of_slot[s];
+            const bool in_buf = s >= b * E && s < b * E + E;
+            if (in_buf) {
+                const int f_new = l * E + (s - b * E);
+                if (f_old >= 0 && f_old != f_new) a.slot_for_id[f_old] = -1;
+            } else if (f_old >= 0 && f_old / E == l) {
+                a.id_of_slot[s] = -1;
+                a.usage[s] = -1;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += 1024) {
+            const int s = b * E + e;
+            a.id_of_slot[s] = l * E + e;
+            a.slot_for_id[l * E + e] = s;
+        }
+        __syncthreads();
+    }
+    // touched = slots of the loaded buffers
+    auto touched = [&](int s) {
+        return (s >= a.ba * E && s < a.ba * E + E) || (a.lb >= 0 && s >= a.bb * E && s < a.bb * E + E);
+    };
+    const int nc = (C + 1023) / 1024;
+    // read the old order before rewriting it
+    int old_loc[kSlotsPerThread];
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        const int pos = tid * nc + j;
+        old_loc[j] = (j < nc && pos < C) ? a.lru_order[pos] : -1;
+    }
+    int n_free = 0, n_keep = 0, n_touch = 0;
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        const int s = tid * nc + j;          // slot-index order (free and touched)
+        if (j < nc && s < C) {
+            if (touched(s)) ++n_touch;
+            else if (a.id_of_slot[s] < 0) ++n_free;
+        }
+        const int so = old_loc[j];           // old LRU order (kept occupied)
+        if (so >= 0 && !touched(so) && a.id_of_slot[so] >= 0) ++n_keep;
+    }
+    int tot_free = 0, tot_keep = 0, tot_touch = 0;
+    int r_free = block_exclusive_scan(n_free, &tot_free, s_scan);
+    int r_keep = block_exclusive_scan(n_keep, &tot_keep, s_scan);
+    int r_touch = block_exclusive_scan(n_touch, &tot_touch, s_scan);
+    const long long tick = s_tick;
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        const int s = tid * nc + j;
+        if (j < nc && s < C) {
+            if (touched(s)) {
+                a.usage[s] = tick;
+                a.lru_order[tot_free + tot_keep + r_touch++] = s;
+            } else if (a.id_of_slot[s] < 0) {
+                a.lru_order[r_free++] = s;
+            }
+        }
+        const int so = old_loc[j];
+        if (so >= 0 && !touched(so) && a.id_of_slot[so] >= 0) a.lru_order[tot_free + r_keep++] = so;
+    }
+}
+
+// ------------------------------------------------------------------ route sort
+// Chunks of 32 tokens.  Count of routes per (chunk, expert); a route with an id
+// outside [0, E) or repeating an id of its own token is masked (status bit).
+__global__ void pf_count_kernel(PrefillArgs a) {
+    extern __shared__ uint32_t s_cnt[];            // [E]
+    const int c = blockIdx.x, E = a.E, k = a.k;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    const int t0 = c * 32, t1 = min(a.T, t0 + 32);
+    int bad = 0;
+    for (int i = threadIdx.x; i < (t1 - t0) * k; i += blockDim.x) {
+        const int r = t0 * k + i;
+        const int e = a.ids[r];
+        bool ok = e >= 0 && e < E;
+        for (int j = 0; ok && j < i % k; ++j) ok = a.ids[r - 1 - j] != e;   // earlier in the row
+        if (ok) atomicAdd(&s_cnt[e], 1u);
+        else bad = 1;
+    }
+    if (bad) atomicOr(&a.sc->status, FT_DEV_BAD_ID);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_cnt[(size_t)c * E + e] = s_cnt[e];
+}
+
+// One CTA of 1024 threads: chunk prefixes per expert (in place), expert offsets,
+// m-tile prefix (128-row tiles per expert).
+__global__ void __launch_bounds__(1024, 1) pf_scan_kernel(PrefillArgs a) {
+    __shared__ int s_scan[33];
+    const int E = a.E, n_chunks = (a.T + 31) / 32;
+    const int ne = (E + 1023) / 1024;
+    int tot[kExpertsPerThread], tiles[kExpertsPerThread];
+    int my_tot = 0, my_tiles = 0;
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        tot[j] = 0;
+        tiles[j] = 0;
+        const int e = threadIdx.x * ne + j;
+        if (j < ne && e < E) {
+            int run = 0;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int v = a.chunk_cnt[(size_t)c * E + e];
+                a.chunk_cnt[(size_t)c * E + e] = run;
+                run += v;
+            }
+            tot[j] = run;
+            tiles[j] = (run + 127) / 128;
+        }
+        my_tot += tot[j];
+        my_tiles += tiles[j];
+    }
+    int all_routes = 0, all_tiles = 0;
+    int off = block_exclusive_scan(my_tot, &all_routes, s_scan);
+    int toff = block_exclusive_scan(my_tiles, &all_tiles, s_scan);
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        const int e = threadIdx.x * ne + j;
+        if (j < ne && e < E) {
+            a.offsets[e] = off;
+            a.mtile_prefix[e] = toff;
+            off += tot[j];
+            toff += tiles[j];
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.offsets[E] = all_routes;
+        a.mtile_prefix[E] = all_tiles;
+    }
+}
+
+// CTA per chunk of 32 tokens: each valid route gets its stable position (routes of
+// one expert in token order) and the quantised x row of its token.
+__global__ void pf_scatter_quant_kernel(PrefillArgs a) {
+    extern __shared__ uint32_t s_mask[];           // [E] token bitmask of this chunk
+    const int c = blockIdx.x, E = a.E, k = a.k, H = a.H;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0;
+    __syncthreads();
+    const int t0 = c * 32, t1 = min(a.T, t0 + 32);
+    for (int i = threadIdx.x; i < (t1 - t0) * k; i += blockDim.x) {
+        const int r = t0 * k + i, e = a.ids[r];
+        bool ok = e >= 0 && e < E;
+        for (int j = 0; ok && j < i % k; ++j) ok = a.ids[r - 1 - j] != e;
+        if (ok) atomicOr(&s_mask[e], 1u << (i / k));
+    }
+    __syncthreads();
+    // positions
+    for (int i = threadIdx.x; i < (t1 - t0) * k; i += blockDim.x) {
+        const int r = t0 * k + i, e = a.ids[r];
+        bool ok = e >= 0 && e < E;
+        for (int j = 0; ok && j < i % k; ++j) ok = a.ids[r - 1 - j] != e;
+        int pos = -1;
+        if (ok) {
+            const int tl = i / k;
+            pos = a.offsets[e] + a.chunk_cnt[(size_t)c * E + e] + __popc(s_mask[e] & ((1u << tl) - 1u));
+            a.perm[pos] = r;
+        }
+        a.route_pos[r] = pos;
+    }
+    __syncthreads();
+    // quantise each token row once, write it to every route position of the token
+    const int nblk = H / 16;
+    for (int i = threadIdx.x; i < (t1 - t0) * nblk; i += blockDim.x) {
+        const int tl = i / nblk, blk = i % nblk, t = t0 + tl;
+        const __nv_bfloat16* xp = a.x + (size_t)t * H + blk * 16;
+        float v[16];
+        const uint4 q0 = *reinterpret_cast<const uint4*>(xp);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(xp + 8);
+        const __nv_bfloat162* b0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
+        const __nv_bfloat162* b1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f0 = __bfloat1622float2(b0[j]), f1 = __bfloat1622float2(b1[j]);
+            v[2 * j] = f0.x; v[2 * j + 1] = f0.y; v[8 + 2 * j] = f1.x; v[8 + 2 * j + 1] = f1.y;
+        }
+        uint32_t lo, hi;
+        const uint8_t sc = quant_block16(v, lo, hi);
+        for (int j = 0; j < k; ++j) {
+            const int pos = a.route_pos[(size_t)t * k + j];
+            if (pos < 0) continue;
+            *reinterpret_cast<uint2*>(a.a_codes + (size_t)pos * (H / 2) + blk * 8) = make_uint2(lo, hi);
+            a.a_scales[(size_t)pos * nblk + blk] = sc;
+        }
+    }
+}
+
+// y[t] = sum_j O[t*k + j] over the token's valid routes, in order j.
+__global__ void pf_combine_kernel(PrefillArgs a) {
+    const int H4 = a.H / 4;
+    const size_t n = (size_t)a.T * H4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / H4), c = (int)(i % H4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < a.k; ++j) {
+            const size_t r = (size_t)t * a.k + j;
+            if (a.route_pos[r] < 0) continue;
+            const float4 o = reinterpret_cast<const float4*>(a.O + r * a.H)[c];
+            acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+        }
+        reinterpret_cast<float4*>(a.y + (size_t)t * a.H)[c] = acc;
+    }
+}
+
+cudaError_t launch_pf_tables(const PrefillTablesArgs& a, cudaStream_t s) {
+    pf_tables_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_sort_quant(const PrefillArgs& a, cudaStream_t s) {
+    const int n_chunks = (a.T + 31) / 32;
+    const size_t sm = (size_t)a.E * 4;
+    pf_count_kernel<<<n_chunks, 256, sm, s>>>(a);
+    pf_scan_kernel<<<1, 1024, 0, s>>>(a);
+    pf_scatter_quant_kernel<<<n_chunks, 256, sm, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_combine(const PrefillArgs& a, cudaStream_t s) {
+    const size_t n = (size_t)a.T * (a.H / 4);
+    size_t grid = (n + 255) / 256;
+    if (grid > (size_t)sm_count() * 8) grid = (size_t)sm_count() * 8;
+    pf_combine_kernel<<<(unsigned)grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ft

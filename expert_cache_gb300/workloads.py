@@ -1,0 +1,114 @@
+"""Workload shapes and device-side setup for the routed-expert cache.
+
+Builds the pinned host expert pool (fp32 weights drawn on the GPU by ``synth``,
+quantised to NVFP4 records by ``ft_quantize_experts``, copied into pinned memory),
+the device-resident shared experts, and the per-step decode inputs.  Nothing here
+computes any part of the hot path.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synth
+from . import (FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR, ExpertCache, PinnedBuffer,
+               ft_moe_decode, ft_quantize_experts, ft_record_bytes)
+
+
+@dataclass
+class Shape:
+    name: str
+    L: int
+    E: int
+    k: int
+    H: int
+    I: int
+    C: int
+    B: int = 1
+    steps: int = 256
+    p: float = 0.8
+    shared: bool = False
+    T: int = 0
+    resize: dict = field(default_factory=dict)   # step -> new capacity
+
+
+# The workloads: a tiny parity case, Qwen3.6-35B-A3B-shaped decode and prefill,
+# DeepSeek-V4-Flash-shaped decode, and the elastic stress run.
+SHAPES = {
+    "tiny": Shape("tiny", L=2, E=16, k=2, H=64, I=32, C=8, B=1, steps=32, p=0.8),
+    "qwen_decode": Shape("qwen_decode", L=40, E=256, k=8, H=2048, I=512, C=600, B=1,
+                         steps=256, p=0.8, shared=True),
+    "dsv4_decode": Shape("dsv4_decode", L=16, E=256, k=6, H=4096, I=2048, C=1024, B=1,
+                         steps=256, p=0.8),
+    "qwen_prefill": Shape("qwen_prefill", L=40, E=256, k=8, H=2048, I=512, C=600, T=8192),
+    "stress": Shape("stress", L=16, E=256, k=6, H=4096, I=2048, C=1024, B=16, steps=512,
+                    p=0.3, resize={171: 256, 342: 768}),
+}
+
+
+def build_pool(seed: int, L: int, E: int, H: int, I: int, chunk_bytes: int = 1 << 30,
+               device: str = "cuda") -> PinnedBuffer:
+    """Pinned host pool of L*E NVFP4 records, flat id l*E + e."""
+    rec = ft_record_bytes(H, I)
+    n_all = L * E
+    pool = PinnedBuffer(n_all * rec)
+    host = pool.tensor()
+    per = max(1, min(n_all, chunk_bytes // (3 * H * I * 4)))
+    stage = torch.empty(per * rec, dtype=torch.uint8, device=device)
+    for f0 in range(0, n_all, per):
+        n = min(per, n_all - f0)
+        w_gu = torch.empty((n, 2 * I, H), dtype=torch.float32, device=device)
+        w_d = torch.empty((n, H, I), dtype=torch.float32, device=device)
+        a, b = synth.expert_weights_batch(seed, f0, n, H, I, device)
+        w_gu.copy_(a)
+        w_d.copy_(b)
+        del a, b
+        ft_quantize_experts(w_gu, w_d, n, H, I, stage)
+        host[f0 * rec:(f0 + n) * rec].copy_(stage[:n * rec])
+    torch.cuda.synchronize()
+    return pool
+
+
+def build_shared(seed: int, L: int, H: int, I: int, device: str = "cuda") -> torch.Tensor:
+    """Device records of the always-resident shared expert of each layer."""
+    rec = ft_record_bytes(H, I)
+    out = torch.empty(L * rec, dtype=torch.uint8, device=device)
+    for l in range(L):
+        a, b = synth.shared_weights(seed, l, H, I, device)
+        ft_quantize_experts(a.contiguous(), b.contiguous(), 1, H, I, out[l * rec:(l + 1) * rec])
+    torch.cuda.synchronize()
+    return out
+
+
+class DecodeWorkload:
+    """Resident decode inputs/outputs of a shape for `steps` steps."""
+
+    def __init__(self, shape: Shape, seed: int = 0, steps: int | None = None, device="cuda"):
+        s = shape
+        self.shape = s
+        self.steps = steps or s.steps
+        self.trace = synth.locality_trace(seed, s.L, s.E, s.k, s.B, self.steps, s.p)
+        self.gates = synth.decode_gates(seed, self.steps, s.L, s.B, s.k)
+        self.ids = torch.from_numpy(self.trace).to(device)
+        self.w = torch.from_numpy(self.gates).to(device)
+        self.x = synth.decode_x_all(seed, self.steps, s.L, s.B, s.H, device)
+        self.y = torch.empty((self.steps, s.L, s.B, s.H), dtype=torch.float32, device=device)
+        self.deferred = torch.empty((self.steps, s.L, s.B, s.k), dtype=torch.int32, device=device)
+        self.route_slot = torch.empty_like(self.deferred)
+        self.counters = torch.empty((self.steps, s.L, 4), dtype=torch.int32, device=device)
+
+    def run_layer(self, cache: ExpertCache, t: int, l: int, stream=None):
+        s = self.shape
+        ft_moe_decode(cache.handle, l, self.x[t, l], self.ids[t, l], self.w[t, l], s.B, s.k,
+                      self.y[t, l], self.deferred[t, l], self.route_slot[t, l],
+                      self.counters[t, l], stream)
+
+    def run_step(self, cache: ExpertCache, t: int, stream=None):
+        for l in range(self.shape.L):
+            self.run_layer(cache, t, l, stream)
+
+
+def split_tuple(mode: str, f_q16: int = 65536):
+    return (FT_SPLIT_FULL_OFFLOAD, 65536) if mode == "full" else (FT_SPLIT_QSTAR, int(f_q16))

@@ -1,0 +1,222 @@
+/*
+ * ft.h -- C ABI of a GB300-native routed-expert cache for MoE layers.
+ *
+ * The full routed-expert pool lives in pinned host memory (the source of truth);
+ * HBM holds a global, cross-layer cache of whole (layer, expert) slots.
+ *
+ * Pages cited (by title; sections as printed on each page):
+ *   [EXPLAINER] "FreeToken: Efficient Edge-Native MoE Serving with Bandwidth-Adaptive
+ *               Execution" (blog explainer of the arXiv v1 paper)
+ *   [QIITA]     "FreeTokenってなんだ？ ─ 8GBノートPCで35Bを動かす判断基準"
+ *   [BWRATIO]   "FreeToken hybrid MoE 后端：带宽比如何决定专家「搬」还是「算」"
+ *   [JUHE]      the juhe.plus article on FreeToken's 8 GB RTX 4060 Laptop result
+ *               (cited by its section headings)
+ *
+ * Conventions
+ *   - Every call returns ft_status; FT_OK is 0.  No C++ exception crosses the ABI.
+ *   - The caller owns all memory: the host pool, the slot buffer, the workspace,
+ *     inputs and outputs.  The library owns only the opaque ft_cache handle, one
+ *     internal copy stream and CUDA events.
+ *   - `stream` arguments are cudaStream_t values passed as void* (NULL = legacy
+ *     default stream).  Per-token calls (ft_moe_decode) are asynchronous on it,
+ *     perform no host synchronisation and no allocation.
+ *   - Pointers marked "device" must be device (or managed) memory of the current
+ *     device; "host" pointers are ordinary host memory; "pinned" means allocated
+ *     with ft_pinned_alloc or otherwise page-locked and mapped.
+ *   - Sizes are element counts unless they end in _bytes.
+ *
+ * Record layout (one per flat id l*E + e; see ft_record_bytes):
+ *   [W_gu codes 2I*H/2][W_gu scales 2I*H/16][W_d codes H*I/2][W_d scales H*I/16]
+ *   [s_gu fp32][s_d fp32], padded to a multiple of 256 bytes.
+ *   W_gu is [2I, H] row-major (gate rows 0..I-1, up rows I..2I-1); W_d is [H, I].
+ *   NVFP4: E2M1 codes, two per byte with element 2j in the low nibble; one unsigned
+ *   E4M3 scale per 16 consecutive elements of a row; one fp32 tensor scale per
+ *   matrix.  value = e2m1(code) * e4m3(scale) * s_t.
+ */
+#ifndef FT_H
+#define FT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ft_status;
+#define FT_OK            0
+#define FT_ERR_ARG       1   /* bad argument (size, layer, pointer, id range) */
+#define FT_ERR_CUDA      2   /* a CUDA runtime call failed */
+#define FT_ERR_CAPACITY  3   /* not enough slots for the requested operation */
+#define FT_ERR_STATE     4   /* call not allowed in the current state (e.g. capturing) */
+#define FT_ERR_TIMEOUT   5   /* a bounded device wait ran out */
+#define FT_ERR_UNPINNED  6   /* host pool is not page-locked / mapped */
+
+/* Bits of the device status word (ft_cache_status). */
+#define FT_DEV_BAD_ID    0x1 /* a route id outside [0, E) was masked */
+#define FT_DEV_TIMEOUT   0x2 /* a bounded device wait ran out */
+
+typedef struct ft_cache ft_cache;
+
+/* Miss split ([EXPLAINER §6.2-6.5]; [BWRATIO "第二层带宽比"]).
+ * FT_SPLIT_FULL_OFFLOAD: every unique miss is filled (q = m).
+ * FT_SPLIT_QSTAR: q follows the Q16 integer rule of [BWRATIO "代码全链路" §3] with
+ *   f_q16 in [1, 65536], then q >= 1 ([EXPLAINER §6.5]), then q <= C - |H|. */
+#define FT_SPLIT_FULL_OFFLOAD 0
+#define FT_SPLIT_QSTAR        1
+typedef struct {
+    int32_t  mode;
+    uint32_t f_q16;
+} ft_split;
+
+typedef struct {
+    int32_t L;              /* MoE layers */
+    int32_t E;              /* routed experts per layer (1..4096) */
+    int32_t H;              /* hidden size, multiple of 64 */
+    int32_t I;              /* expert intermediate size, multiple of 32 */
+    int32_t k_max;          /* largest top-k passed to ft_moe_decode (1..32) */
+    int32_t B_max;          /* largest decode batch (1..32) */
+    int32_t capacity;       /* slots C at creation (1..16384) */
+    int32_t capacity_max;   /* largest C ever used by ft_cache_resize (0 = capacity) */
+    int32_t T_max;          /* largest prefill chunk in tokens (0 = no prefill) */
+    const void* host_pool;  /* pinned, L*E records of ft_record_bytes(H, I) bytes */
+    void* slot_buf;         /* device, capacity * record_bytes */
+    void* workspace;        /* device, workspace_bytes from ft_cache_required_sizes;
+                               holds the slot tables; contents are owned by the cache */
+    const void* shared_experts; /* device, L records (always-resident shared expert,
+                               weight 1, [JUHE "先纠正一个容易混淆的模型"]), or NULL */
+    ft_split split;
+} ft_cache_desc;
+
+/* Bytes of one expert record (padded), for hidden H and intermediate I. */
+ft_status ft_record_bytes(int32_t H, int32_t I, size_t* bytes);
+
+/* Record bytes and device workspace bytes needed by a descriptor (host pointers in
+ * it are ignored).  The workspace holds the slot tables ([JUHE "生成阶段"]:
+ * slot_for_id, id_of_slot, usage), the per-call route and work lists, the h
+ * activations and, when T_max > 0, the prefill buffers. */
+ft_status ft_cache_required_sizes(const ft_cache_desc* d, size_t* record_bytes,
+                                  size_t* workspace_bytes);
+
+/* Create a cache over caller-owned memory.  Synchronous.  The cache starts cold
+ * (every slot free, tick 0; [EXPLAINER §7.3]).  Errors: FT_ERR_ARG (sizes, NULL
+ * pointers, misaligned buffers), FT_ERR_UNPINNED (host_pool not page-locked),
+ * FT_ERR_CUDA. */
+ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out);
+void      ft_cache_destroy(ft_cache* c);
+
+/* Safe-point rebuild ([EXPLAINER §7.2]; [JUHE "显存还要在专家缓存和 KV Cache 之间
+ * 动态分配"]): synchronises `stream` and the internal copy stream, switches to
+ * new_capacity slots in new_slot_buf (may equal the old buffer), empties every
+ * table and keeps the host pool; the tick keeps counting.  Errors: FT_ERR_ARG
+ * (new_capacity outside [1, capacity_max] or NULL buffer), FT_ERR_STATE (stream is
+ * being captured), FT_ERR_CUDA. */
+ft_status ft_cache_resize(ft_cache* c, int32_t new_capacity, void* new_slot_buf,
+                          void* stream);
+
+/* Replace the miss split used by later calls.  FT_ERR_ARG on a bad mode/f_q16. */
+ft_status ft_set_split(ft_cache* c, ft_split s);
+
+/* f = min(1, B_P / B_H) as Q16 ([EXPLAINER §6.5]), floor(f*65536 + 0.5); returns 0
+ * when either bandwidth is <= 0. */
+uint32_t  ft_split_from_bandwidth(double B_P, double B_H);
+/* f = p_ov / (p_ov + c_ov) as Q16 ([BWRATIO "实测版本"]); 0 on invalid input. */
+uint32_t  ft_split_from_overlap(double p_ov, double c_ov);
+
+/* One routed-MoE layer of decode ([EXPLAINER §6.1-6.8, §8.2]; [BWRATIO "代码全链路"
+ * §2]; [JUHE "生成阶段"]), fully on the device, in stream order:
+ *   1. flat = layer*E + id for every route; dedupe across the batch (ascending);
+ *   2. hit iff slot_for_id[flat] >= 0; |H| hits, m unique misses;
+ *   3. q from the split, capped at C - |H|;
+ *   4. the q LRU slots not touched by this call (free slots first, ascending, then
+ *      ascending (usage, slot)) take the first q misses in ascending flat id;
+ *      evicted ids are unmapped; every touched slot gets usage = tick (one tick per
+ *      call, touched slots ordered by slot index);
+ *   5. the q fills are read from the pinned pool once, written into their slots and
+ *      computed on the way (load-through over the host link);
+ *   6. NVFP4 SwiGLU per unique GPU expert (hits + fills, + the shared expert);
+ *   7. y[b] = sum_j w[b,j] * o_(b,j) over GPU routes in order j, + shared(x_b).
+ * Arguments:
+ *   x          device bf16 [B, H]
+ *   topk_ids   device int32 [B, k], local expert ids; an id outside [0, E) masks the
+ *              route (neither hit, miss nor deferred) and sets FT_DEV_BAD_ID
+ *   topk_w     device fp32 [B, k] gates
+ *   y          device fp32 [B, H], overwritten (GPU partial: routes on the host share
+ *              contribute 0)
+ *   deferred   device int32 [B, k]: flat id of each route left to the host share
+ *              ([EXPLAINER §6.2] set C), else -1
+ *   route_slot device int32 [B, k] or NULL: slot used by each route, else -1
+ *   counters   device int32 [4] or NULL: n_hit (|H|), m, q, deferred routes
+ * Errors (host-side, nothing launched): FT_ERR_ARG for layer outside [0, L),
+ * B outside [1, B_max], k outside [1, k_max] or NULL x/ids/w/y/deferred. */
+ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t* topk_ids,
+                        const float* topk_w, int32_t B, int32_t k, float* y,
+                        int32_t* deferred, int32_t* route_slot, int32_t* counters,
+                        void* stream);
+
+/* Prefill of one layer over a T-token chunk ([EXPLAINER §4.1-4.3]; [JUHE "Prefill 为什么
+ * 不能也按需加载"]).  With FT_PREFILL_DOUBLE_BUFFER the layer's experts sit in buffer
+ * (layer mod 2) = slots [(layer%2)*E, +E) and, while this layer computes, every
+ * expert of layer+1 streams into the other buffer on the internal copy stream;
+ * capacity must be >= 2E (else FT_ERR_CAPACITY).  Without it only buffer 0 is used
+ * and each layer is loaded before it computes.  Activations and h are NVFP4 (unit
+ * tensor scale, E4M3 per 16); the two grouped GEMMs run on tcgen05 block-scaled
+ * FP4 tensor cores; y[t] = sum_j w[t,j] * o_(t,j) in order j.
+ *   x         device bf16 [T, H];  topk_ids device int32 [T, k];  topk_w device fp32 [T, k]
+ *   y         device fp32 [T, H], overwritten
+ *   debug_h   device uint8 or NULL: per route r = t*k + j, I/2 packed h codes followed
+ *             (after all T*k rows) by [T*k, I/16] h scales
+ * Calls for one chunk go layer 0, 1, ..., L-1 on the same stream. */
+#define FT_PREFILL_DOUBLE_BUFFER 1
+ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void* x,
+                               const int32_t* topk_ids, const float* topk_w, int32_t T,
+                               int32_t k, float* y, int32_t flags, void* debug_h,
+                               void* stream);
+
+/* Copy the tables to host arrays (synchronises the cache's streams):
+ * slot_for_id [L*E], id_of_slot [C], usage [C] (-1 = never used since the last
+ * resize), tick.  Any output may be NULL. */
+ft_status ft_cache_snapshot(ft_cache* c, int32_t* slot_for_id, int32_t* id_of_slot,
+                            int64_t* usage, int64_t* tick);
+
+/* Current slot count. */
+ft_status ft_cache_capacity(const ft_cache* c, int32_t* capacity);
+
+/* Read and clear the device status word (FT_DEV_* bits).  Synchronises. */
+ft_status ft_cache_status(ft_cache* c, int32_t* device_status);
+
+/* Quantise n experts to NVFP4 records on the device ([EXPLAINER §8.4] layout; the
+ * quantiser of the record format above, fp32 IEEE steps):
+ *   s_t = amax(W)/2688; block scale = E4M3_RNE((amax16/6)/s_t);
+ *   code = E2M1_RNE_sat(w / (scale*s_t)); a zero scale gives a zero block.
+ *   w_gu device fp32 [n, 2I, H];  w_d device fp32 [n, H, I];
+ *   records device uint8 [n, ft_record_bytes(H, I)]. */
+ft_status ft_quantize_experts(const float* w_gu, const float* w_d, int32_t n, int32_t H,
+                              int32_t I, void* records, void* stream);
+
+/* Page-locked, device-mapped host memory for the pool ([EXPLAINER §7.3]: pin the
+ * pool; the caller fills it). */
+ft_status ft_pinned_alloc(size_t bytes, void** out);
+ft_status ft_pinned_free(void* p);
+
+/* Effective pinned-host -> device bandwidth in GB/s ([EXPLAINER §6.3] B_P; [QIITA §7]):
+ * best of `reps` timed cudaMemcpyAsync of `bytes` from `pinned` to `dev`. */
+ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t reps,
+                         double* gbps);
+
+/* Per-kernel device time accumulated while profiling is on (CUDA events around
+ * each launch on the launching stream).  kind: 0 remap, 1 expert gate/up + fills,
+ * 2 expert down + combine, 3 prefill GEMM1, 4 prefill GEMM2, 5 prefill other. */
+#define FT_PROF_KINDS 6
+ft_status ft_profile_enable(ft_cache* c, int32_t enable);
+ft_status ft_profile_read(ft_cache* c, double* total_ms /*[FT_PROF_KINDS]*/,
+                          int64_t* launches /*[FT_PROF_KINDS]*/);
+
+const char* ft_status_string(ft_status s);
+/* Message of the last failed call on c (static storage), or "" */
+const char* ft_last_error(const ft_cache* c);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_H */

@@ -85,12 +85,29 @@ def gaussian(keys, shape, std: float, device="cpu") -> torch.Tensor:
     return _table(std, device)[idx].reshape(shape)
 
 
+def gaussian_batch(key_list, shape, std: float, device="cpu") -> torch.Tensor:
+    """Stack of gaussian(keys, shape) for every keys pair of key_list, in one pass."""
+    n = int(np.prod(shape))
+    assert n % 2 == 0
+    k = torch.tensor(key_list, dtype=torch.int64, device=device)      # [m, 2]
+    i = torch.arange(n // 2, dtype=torch.int64, device=device)[None, :]
+    h = _hash32(_hash32(i ^ k[:, :1]) ^ k[:, 1:])
+    idx = torch.stack((h & 0xFFFF, h >> 16), dim=2).reshape(len(key_list), n)
+    return _table(std, device)[idx].reshape((len(key_list),) + tuple(shape))
+
+
 # ------------------------------------------------------------- weights / inputs
 
 def expert_weights(seed: int, flat_id: int, H: int, I: int, device="cpu"):
     """(W_gu [2I, H], W_d [H, I]) fp32, N(0, 0.02^2)-shaped, for one routed expert."""
     return (gaussian(key(seed, 1, flat_id, 0), (2 * I, H), 0.02, device),
             gaussian(key(seed, 1, flat_id, 1), (H, I), 0.02, device))
+
+
+def expert_weights_batch(seed: int, flat0: int, n: int, H: int, I: int, device="cpu"):
+    """expert_weights of flat ids flat0 .. flat0+n-1 as [n, 2I, H] and [n, H, I]."""
+    return (gaussian_batch([key(seed, 1, f, 0) for f in range(flat0, flat0 + n)], (2 * I, H), 0.02, device),
+            gaussian_batch([key(seed, 1, f, 1) for f in range(flat0, flat0 + n)], (H, I), 0.02, device))
 
 
 def shared_weights(seed: int, layer: int, H: int, I: int, device="cpu"):
@@ -101,6 +118,12 @@ def shared_weights(seed: int, layer: int, H: int, I: int, device="cpu"):
 def decode_x(seed: int, step: int, layer: int, L: int, B: int, H: int, device="cpu"):
     """bf16 [B, H] activations of one (step, layer), N(0, 1)-shaped."""
     return gaussian(key(seed, 3, step * L + layer), (B, H), 1.0, device).to(torch.bfloat16)
+
+
+def decode_x_all(seed: int, steps: int, L: int, B: int, H: int, device="cpu"):
+    """decode_x of every (step, layer) as one bf16 [steps, L, B, H] tensor."""
+    keys = [key(seed, 3, t * L + l) for t in range(steps) for l in range(L)]
+    return gaussian_batch(keys, (B, H), 1.0, device).to(torch.bfloat16).reshape(steps, L, B, H)
 
 
 def prefill_x(seed: int, layer: int, T: int, H: int, device="cpu"):
