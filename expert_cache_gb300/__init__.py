@@ -66,6 +66,9 @@ _f = {
     "ft_moe_decode": _sig("ft_moe_decode", c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                           c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                           c_void_p),
+    "ft_moe_decode_static": _sig("ft_moe_decode_static", c_int32, c_void_p, c_int32, c_void_p,
+                                 c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p),
     "ft_moe_prefill_layer": _sig("ft_moe_prefill_layer", c_int32, c_void_p, c_int32, c_void_p,
                                  c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                  c_void_p, c_void_p),
@@ -165,6 +168,13 @@ def ft_moe_decode(handle, layer, x, topk_ids, topk_w, B, k, y, deferred, route_s
     _check(_f["ft_moe_decode"](handle, layer, _ptr(x), _ptr(topk_ids), _ptr(topk_w), B, k,
                                _ptr(y), _ptr(deferred), _ptr(route_slot), _ptr(counters),
                                _stream(stream)), handle)
+
+
+def ft_moe_decode_static(handle, layer, x, topk_ids, topk_w, B, k, y, deferred, route_slot=None,
+                         counters=None, stream=None):
+    _check(_f["ft_moe_decode_static"](handle, layer, _ptr(x), _ptr(topk_ids), _ptr(topk_w), B, k,
+                                      _ptr(y), _ptr(deferred), _ptr(route_slot), _ptr(counters),
+                                      _stream(stream)), handle)
 
 
 def ft_moe_prefill_layer(handle, layer, x, topk_ids, topk_w, T, k, y, flags=FT_PREFILL_DOUBLE_BUFFER,

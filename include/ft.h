@@ -154,6 +154,22 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
                         int32_t* deferred, int32_t* route_slot, int32_t* counters,
                         void* stream);
 
+/* ft_moe_decode with no allocation and no per-call workspace: the same layer call
+ * (same arguments, same results, same cache state) whose per-call scratch lives in
+ * a static 8 MiB device array built into the library instead of the workspace.
+ * The paper has no counterpart; it serves callers that cannot allocate device
+ * memory (a host framework that owns all device memory through its own pool, or a
+ * serving loop that must never enter the CUDA allocator).  The array's device
+ * address is looked up on the first call made on each device, so make that first
+ * call before any stream capture.  Every call shares the array: calls that
+ * overlap on the GPU race and must be serialised by the caller.  Errors: those of
+ * ft_moe_decode, and FT_ERR_ARG when B, k, H and I need more than 8 MiB of
+ * scratch (about (B*k + B) * (H + I) * 4 bytes). */
+ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
+                               const int32_t* topk_ids, const float* topk_w, int32_t B,
+                               int32_t k, float* y, int32_t* deferred, int32_t* route_slot,
+                               int32_t* counters, void* stream);
+
 /* Prefill of one layer over a T-token chunk ([EXPLAINER §4.1-4.3]; [JUHE "Prefill 为什么
  * 不能也按需加载"]).  With FT_PREFILL_DOUBLE_BUFFER the layer's experts sit in buffer
  * (layer mod 2) = slots [(layer%2)*E, +E) and, while this layer computes, every
