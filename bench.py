@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-chunks", type=int, default=2)
     return ap.parse_args()
 
 
@@ -333,8 +335,82 @@ def native_decode(args, rank, world):
                                "sample": f"{calls} decode layer calls of this workload (state "
                                          f"oracle + fp64 outputs), extrapolated to {s.L} layers"}
     cache.close()
+    if not args.no_prefill and s.H % 256 == 0 and s.I % 256 == 0:
+        out["prefill"] = native_prefill(args, pool, b_p, hbm_gbs, world)
     pool.free()
     return out
+
+
+def native_prefill(args, pool, b_p, hbm_gbs, world):
+    """Qwen3.6-shaped prefill: one 8192-token chunk through 40 layers, the next layer
+    streaming into the other full-layer buffer while the current one computes (and,
+    for comparison, without the double buffer)."""
+    import torch
+    import expert_cache_gb300 as ft
+    import synth
+    from expert_cache_gb300.workloads import SHAPES
+    s = SHAPES["qwen_prefill"]
+    T, L = s.T, s.L
+    rec = ft.ft_record_bytes(s.H, s.I)
+    cache = ft.ExpertCache(L, s.E, s.H, s.I, s.k, 1, s.C, pool.ptr, T_max=T)
+    xs = [synth.prefill_x(args.seed, l, T, s.H, "cuda") for l in range(L)]
+    routes = [synth.prefill_routes(args.seed, l, T, s.E, s.k, "cuda") for l in range(L)]
+    y = torch.empty((T, s.H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def chunk(flags):
+        for l in range(L):
+            ids, gates = routes[l]
+            ft.ft_moe_prefill_layer(cache.handle, l, xs[l], ids, gates, T, s.k, y, flags)
+
+    res = {}
+    for name, flags in (("double_buffer", ft.FT_PREFILL_DOUBLE_BUFFER), ("single_buffer", 0)):
+        chunk(flags)                                   # warm-up chunk
+        torch.cuda.synchronize()
+        barrier(world)
+        if name == "double_buffer":
+            ft.ft_profile_enable(cache.handle, True)
+            ft.ft_profile_read(cache.handle)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.prefill_chunks):
+            chunk(flags)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.prefill_chunks
+        if name == "double_buffer":
+            prof = ft.ft_profile_read(cache.handle)
+            ft.ft_profile_enable(cache.handle, False)
+        res[name] = {"ms_per_chunk": ms, "tok_s": T * world / (ms / 1e3)}
+    assert ft.ft_cache_status(cache.handle) == 0
+    cache.close()
+    link_ms = L * s.E * rec / (b_p * 1e9) * 1e3
+    flops = 2.0 * T * s.k * 3 * s.H * s.I * L
+    _, bf16_tf, src = peaks()
+    fp4_tf = bf16_tf * 6.0                              # nominal dense FP4 : BF16 ratio (13.5 / 2.25)
+    comp_ms = flops / (fp4_tf * 1e12) * 1e3
+    roof_ms = max(link_ms, comp_ms)
+    g1_ms, g1_n = prof["prefill_gemm1"]
+    g2_ms, g2_n = prof["prefill_gemm2"]
+    g1_flop = 2.0 * T * s.k * 2 * s.I * s.H
+    g2_flop = 2.0 * T * s.k * s.H * s.I
+    return {
+        "workload": s.name, "T": T, "L": L, "capacity": s.C,
+        "tok_s": res["double_buffer"]["tok_s"],
+        "ms_per_chunk": res["double_buffer"]["ms_per_chunk"],
+        "tok_s_single_buffer": res["single_buffer"]["tok_s"],
+        "ms_per_chunk_single_buffer": res["single_buffer"]["ms_per_chunk"],
+        "roofline": {"bound": "host link (streamed bytes) vs FP4 tensor", "link_ms": link_ms,
+                     "compute_ms_at_peak": comp_ms, "frac": roof_ms / res["double_buffer"]["ms_per_chunk"],
+                     "streamed_bytes": L * s.E * rec, "b_p_gbs": b_p,
+                     "fp4_peak_tflops": fp4_tf, "fp4_peak_source": f"{src} bf16 x 6 (nominal ratio)"},
+        "gemm": {"gemm1_tflops": g1_flop / (g1_ms / g1_n / 1e3) / 1e12 if g1_n else None,
+                 "gemm2_tflops": g2_flop / (g2_ms / g2_n / 1e3) / 1e12 if g2_n else None,
+                 "gemm1_ms_per_layer": g1_ms / g1_n if g1_n else None,
+                 "gemm2_ms_per_layer": g2_ms / g2_n if g2_n else None,
+                 "other_ms_per_layer": prof["prefill_other"][0] / max(g1_n, 1)},
+    }
 
 
 def native_e2e(args, s, wl, cache, stream, world):

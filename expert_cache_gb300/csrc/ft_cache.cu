@@ -4,9 +4,11 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <new>
 
 #include "ft_internal.cuh"
+#include "ft_umma.cuh"
 
 namespace ft {
 
@@ -30,8 +32,20 @@ WsLayout ws_layout(const ft_cache_desc& d) {
     w.h = take(P * (size_t)d.I * 4);
     w.o = take(P * (size_t)d.H * 4);
     w.tile_done = take((size_t)(d.H / kDownRowsPerItem + 1) * 4);
-    w.prefill = off;
-    w.prefill_bytes = 0;
+    if (d.T_max > 0) {
+        // at least one 128-row tile so a TMA box never exceeds the sorted buffers
+        const size_t RT = std::max<size_t>((size_t)d.T_max * d.k_max, 128);
+        w.pf_chunk_cnt = take((size_t)((d.T_max + 31) / 32) * d.E * 4);
+        w.pf_offsets = take((size_t)(d.E + 1) * 4);
+        w.pf_mtile = take((size_t)(d.E + 1) * 4);
+        w.pf_perm = take(RT * 4);
+        w.pf_route_pos = take(RT * 4);
+        w.pf_a_codes = take(RT * d.H / 2);
+        w.pf_a_scales = take(RT * d.H / 16);
+        w.pf_h_codes = take(RT * d.I / 2);
+        w.pf_h_scales = take(RT * d.I / 16);
+        w.pf_o = take(RT * d.H * 4);
+    }
     w.total = off;
     return w;
 }
@@ -79,6 +93,21 @@ static ft_status check_desc(const ft_cache_desc* d) {
     if (d->split.mode != FT_SPLIT_FULL_OFFLOAD && d->split.mode != FT_SPLIT_QSTAR) return FT_ERR_ARG;
     if (d->split.mode == FT_SPLIT_QSTAR && (d->split.f_q16 < 1 || d->split.f_q16 > 65536)) return FT_ERR_ARG;
     return FT_OK;
+}
+
+// TMA maps of the prefill GEMM operands (only when the cache supports prefill).
+static bool prefill_maps(ft_cache* c) {
+    const ft_cache_desc& d = c->d;
+    if (d.T_max <= 0 || d.H % 256 || d.I % 256) return false;
+    const uint64_t RT = std::max<uint64_t>((uint64_t)d.T_max * d.k_max, 128);
+    uint8_t* ws = c->workspace;
+    bool ok = make_map_2d(&c->map_a1, ws + c->ws.pf_a_codes, d.H / 2, RT);
+    ok = ok && make_map_2d(&c->map_a2, ws + c->ws.pf_h_codes, d.I / 2, RT);
+    ok = ok && make_map_3d(&c->map_b1, c->slot_buf + c->rec.gu_codes, d.H / 2, 2 * (uint64_t)d.I,
+                           (uint64_t)c->C, c->rec.bytes, 128);
+    ok = ok && make_map_3d(&c->map_b2, c->slot_buf + c->rec.d_codes, d.I / 2, (uint64_t)d.H,
+                           (uint64_t)c->C, c->rec.bytes, 256);
+    return ok;
 }
 
 extern "C" {
@@ -148,6 +177,8 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
         cudaEventCreateWithFlags(&c->copy_done[i], cudaEventDisableTiming);
         cudaEventCreateWithFlags(&c->compute_done[i], cudaEventDisableTiming);
     }
+    cudaEventCreateWithFlags(&c->entry_ev, cudaEventDisableTiming);
+    c->maps_ok = prefill_maps(c);
     uint8_t* ws = c->workspace;
     e = launch_init_tables(reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id), d->L * d->E,
                            reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot),
@@ -170,6 +201,7 @@ void ft_cache_destroy(ft_cache* c) {
         cudaEventDestroy(c->copy_done[i]);
         cudaEventDestroy(c->compute_done[i]);
     }
+    cudaEventDestroy(c->entry_ev);
     if (c->prof_n >= 0) {
         for (int i = 0; i < ft_cache::kProfEvents; ++i)
             if (c->prof_ev[i]) cudaEventDestroy(c->prof_ev[i]);
@@ -349,6 +381,7 @@ ft_status ft_cache_resize(ft_cache* c, int32_t new_capacity, void* new_slot_buf,
     if (e != cudaSuccess) return cuda_fail(c, e, "resize drain");
     c->C = new_capacity;
     c->slot_buf = static_cast<uint8_t*>(new_slot_buf);
+    c->maps_ok = prefill_maps(c);
     c->buffer_layer[0] = c->buffer_layer[1] = -1;
     c->copy_pending = false;
     uint8_t* ws = c->workspace;

@@ -1,6 +1,7 @@
 // Internal declarations of the expert-cache library (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -76,8 +77,9 @@ struct Unit {
 struct WsLayout {
     size_t slot_for_id, id_of_slot, usage, lru_order, scalars;
     size_t units, route_pair, pair_tok, h, o, tile_done;
-    size_t prefill;        // start of the prefill region (0 bytes if T_max == 0)
-    size_t prefill_bytes;
+    // prefill region (present when T_max > 0)
+    size_t pf_chunk_cnt, pf_offsets, pf_mtile, pf_perm, pf_route_pos;
+    size_t pf_a_codes, pf_a_scales, pf_h_codes, pf_h_scales, pf_o;
     size_t total;
 };
 
@@ -175,6 +177,10 @@ struct ft_cache {
     cudaEvent_t compute_done[2];    // prefill buffer no longer read
     int buffer_layer[2];            // layer last streamed into each prefill buffer (-1 none)
     bool copy_pending;
+    cudaEvent_t entry_ev;           // work enqueued before a prefill call
+    CUtensorMap map_a1, map_b1;     // GEMM1: quantised x rows; W_gu codes of the slots
+    CUtensorMap map_a2, map_b2;     // GEMM2: quantised h rows; W_d codes of the slots
+    bool maps_ok;
     int grid_gemv;
     // profiling
     bool prof;
