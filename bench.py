@@ -202,7 +202,8 @@ def native_decode(args, rank, world):
     import numpy as np
     import torch
     import expert_cache_gb300 as ft
-    from expert_cache_gb300.workloads import SHAPES, DecodeWorkload, build_pool, build_shared, split_tuple
+    from expert_cache_gb300.workloads import (SHAPES, DecodeWorkload, StepGraph, build_pool, build_shared,
+                                              split_tuple)
 
     s = SHAPES[args.workload]
     if args.p is not None:
@@ -226,13 +227,23 @@ def native_decode(args, rank, world):
     stream = torch.cuda.current_stream()
     hbm_gbs, _, peak_src = peaks()
 
-    def run(t0, t1):
+    graph = StepGraph(wl, cache)
+
+    def run(t0, t1, use_graph):
         for t in range(t0, t1):
-            wl.run_step(cache, t)
+            if use_graph:
+                graph.replay(t)
+            else:
+                wl.run_step(cache, t)
 
     def timed(profile=False):
+        # value: each step is one CUDA-graph replay of the 40 layer calls (inputs of the
+        # step copied into the graph's buffers, outputs copied out); the profiling pass
+        # runs the same steps eagerly with CUDA events around every kernel
         ft.ft_cache_resize(cache.handle, s.C, cache.slot_buf)   # empty cache, same trace
-        run(0, args.warmup)
+        run(0, args.warmup, False)
+        if not profile and graph.graph is None:
+            graph.capture()
         if profile:
             ft.ft_profile_enable(cache.handle, True)
             ft.ft_profile_read(cache.handle)
@@ -240,7 +251,7 @@ def native_decode(args, rank, world):
         barrier(world)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        run(args.warmup, steps)
+        run(args.warmup, steps, not profile)
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -323,11 +334,12 @@ def native_decode(args, rank, world):
         "roofline": roofline,
         "kernels": kernels,
         "gpu_launches": 3 * launches,
+        "step_execution": "one CUDA graph replay per step (40 layer calls, 3 kernels each)",
         "clocks": clk.summary(),
     }
 
     if not args.no_e2e:
-        out["e2e"] = native_e2e(args, s, wl, cache, stream, world)
+        out["e2e"] = native_e2e(args, s, wl, cache, graph, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sec, calls = oracle_decode_sample(s, args.seed, wl.trace, wl.gates, budget_s=20.0)
         out["cpu_baseline"] = {"value": 1.0 / (sec * s.L) * s.B, "unit": "tok/s", "cores": 1,
@@ -413,9 +425,9 @@ def native_prefill(args, pool, b_p, hbm_gbs, world):
     }
 
 
-def native_e2e(args, s, wl, cache, stream, world):
-    """Same steps through the C ABI with the step's inputs in pinned host memory:
-    H2D of x/ids/gates and D2H of y inside the timed region."""
+def native_e2e(args, s, wl, cache, graph, stream, world):
+    """Same steps through the C ABI (the captured step graph) with the step's inputs
+    in pinned host memory: H2D of x/ids/gates and D2H of y inside the timed region."""
     import torch
     import expert_cache_gb300 as ft
     steps = args.warmup + args.steps
@@ -423,23 +435,18 @@ def native_e2e(args, s, wl, cache, stream, world):
     hid = wl.ids.cpu().pin_memory()
     hw = wl.w.cpu().pin_memory()
     hy = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
-    dx = torch.empty_like(wl.x[0])
-    di = torch.empty_like(wl.ids[0])
-    dw = torch.empty_like(wl.w[0])
-    dy = torch.empty_like(wl.y[0])
-    dd = torch.empty_like(wl.deferred[0])
+    dx, di, dw, dy = graph.x, graph.ids, graph.w, graph.y
 
     def step(t):
         dx.copy_(hx[t], non_blocking=True)
         di.copy_(hid[t], non_blocking=True)
         dw.copy_(hw[t], non_blocking=True)
-        for l in range(s.L):
-            ft.ft_moe_decode(cache.handle, l, dx[l], di[l], dw[l], s.B, s.k, dy[l], dd[l], None, None)
+        graph.graph.replay()
         hy[t].copy_(dy, non_blocking=True)
 
     ft.ft_cache_resize(cache.handle, s.C, cache.slot_buf)
     for t in range(args.warmup):
-        step(t)
+        wl.run_step(cache, t)
     torch.cuda.synchronize()
     barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

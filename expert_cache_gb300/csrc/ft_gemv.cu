@@ -109,6 +109,7 @@ __device__ __forceinline__ float ldcg_f(const float* p) {
 
 __global__ void __launch_bounds__(kGemvThreads) gate_up_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    pdl_wait_and_release();
     uint4* xs = reinterpret_cast<uint4*>(smem);          // [kTokGroup][H/8] pieces
     __shared__ unsigned s_item;
     __shared__ int s_tok[kTokGroup];
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kGemvThreads) gate_up_kernel(DecodeArgs a) {
 
 __global__ void __launch_bounds__(kGemvThreads) down_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    pdl_wait_and_release();
     float4* hs = reinterpret_cast<float4*>(smem);         // [kTokGroup][I/4] pieces
     __shared__ unsigned s_item;
     __shared__ int s_last;
@@ -466,13 +468,11 @@ cudaError_t launch_gate_up(const DecodeArgs& a, int grid, cudaStream_t s) {
         cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
         attr_set = true;
     }
-    gate_up_kernel<<<grid, kGemvThreads, sm, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gate_up_kernel, dim3(grid), dim3(kGemvThreads), sm, s, a);
 }
 
 cudaError_t launch_down(const DecodeArgs& a, int grid, cudaStream_t s) {
-    down_kernel<<<grid, kGemvThreads, down_smem(a.I), s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(down_kernel, dim3(grid), dim3(kGemvThreads), down_smem(a.I), s, a);
 }
 
 int gemv_occupancy(int H, int I) {

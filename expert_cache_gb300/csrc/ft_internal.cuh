@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <utility>
 
 #include "../../include/ft.h"
 
@@ -160,7 +161,33 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* buf)
     return base + incl - v;
 }
 
+// Programmatic dependent launch: wait until the previous kernel of the stream has
+// completed and its writes are visible (returns at once when this kernel was not
+// launched as a dependent), then allow the next kernel to be scheduled; it waits in
+// turn for this one.
+__device__ __forceinline__ void pdl_wait_and_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 #endif  // __CUDACC__
+
+// Launch with programmatic stream serialisation (see pdl_wait_and_release).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace ft
 

@@ -45,15 +45,30 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     const int b = db ? layer % 2 : 0;
     cudaError_t e = cudaSuccess;
 
+    // whole-layer copy host pool -> buffer on the copy stream, after everything enqueued
+    // on the caller's stream before this call (the last reader of the buffer)
+    auto copy_layer = [&](int l, int buf) -> cudaError_t {
+        cudaStreamWaitEvent(c->copy_stream, c->entry_ev, 0);
+        cudaEvent_t e1 = nullptr;
+        if (c->prof && c->prof_n * 2 + 2 <= ft_cache::kProfEvents) {
+            const int i = c->prof_n++;
+            c->prof_kind[i] = 6;
+            cudaEventRecord(c->prof_ev[2 * i], c->copy_stream);
+            e1 = c->prof_ev[2 * i + 1];
+        }
+        cudaError_t r = cudaMemcpyAsync(c->slot_buf + (size_t)buf * layer_bytes,
+                                        host + (size_t)l * layer_bytes, layer_bytes,
+                                        cudaMemcpyHostToDevice, c->copy_stream);
+        if (e1) cudaEventRecord(e1, c->copy_stream);
+        cudaEventRecord(c->copy_done[buf], c->copy_stream);
+        c->buffer_layer[buf] = l;
+        return r;
+    };
+
     // 1. layer -> buffer b (already there when the previous call prefetched it)
     cudaEventRecord(c->entry_ev, s);
     if (c->buffer_layer[b] != layer) {
-        cudaStreamWaitEvent(c->copy_stream, c->entry_ev, 0);
-        e = cudaMemcpyAsync(c->slot_buf + (size_t)b * layer_bytes, host + (size_t)layer * layer_bytes,
-                            layer_bytes, cudaMemcpyHostToDevice, c->copy_stream);
-        if (e != cudaSuccess) return fail(FT_ERR_CUDA, "layer copy");
-        cudaEventRecord(c->copy_done[b], c->copy_stream);
-        c->buffer_layer[b] = layer;
+        if ((e = copy_layer(layer, b)) != cudaSuccess) return fail(FT_ERR_CUDA, "layer copy");
     }
     cudaStreamWaitEvent(s, c->copy_done[b], 0);
 
@@ -74,12 +89,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
 
     // 3. stream layer+1 into the other buffer while this layer computes
     if (lb >= 0 && c->buffer_layer[1 - b] != lb) {
-        cudaStreamWaitEvent(c->copy_stream, c->entry_ev, 0);
-        e = cudaMemcpyAsync(c->slot_buf + (size_t)(1 - b) * layer_bytes, host + (size_t)lb * layer_bytes,
-                            layer_bytes, cudaMemcpyHostToDevice, c->copy_stream);
-        if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefetch copy");
-        cudaEventRecord(c->copy_done[1 - b], c->copy_stream);
-        c->buffer_layer[1 - b] = lb;
+        if ((e = copy_layer(lb, 1 - b)) != cudaSuccess) return fail(FT_ERR_CUDA, "prefetch copy");
         c->copy_pending = true;
     }
 

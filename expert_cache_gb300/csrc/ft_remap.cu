@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kThreadsRemap, 1) remap_kernel(DecodeArgs a) {
     __shared__ int s_scan[33];
     __shared__ int s_q, s_ndef;
 
+    pdl_wait_and_release();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, C = a.C, R = a.B * a.k, layer = a.layer;
     const int base_id = layer * E;
@@ -334,8 +335,7 @@ cudaError_t launch_remap(const DecodeArgs& a, cudaStream_t s) {
                              (int)remap_smem(kMaxE));
         attr = true;
     }
-    remap_kernel<<<1, kThreadsRemap, remap_smem(a.E), s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(remap_kernel, dim3(1), dim3(kThreadsRemap), remap_smem(a.E), s, a);
 }
 
 }  // namespace ft

@@ -99,15 +99,67 @@ class DecodeWorkload:
         self.route_slot = torch.empty_like(self.deferred)
         self.counters = torch.empty((self.steps, s.L, 4), dtype=torch.int32, device=device)
 
+        # raw addresses and per-(step, layer) strides: the per-layer call does integer
+        # arithmetic only (no tensor views on the launch path)
+        self._base = [(tsr.data_ptr(), tsr[0, 0].numel() * tsr.element_size())
+                      for tsr in (self.x, self.ids, self.w, self.y, self.deferred,
+                                  self.route_slot, self.counters)]
+
+    def addresses(self, t: int, l: int):
+        i = t * self.shape.L + l
+        return [b + i * st for b, st in self._base]
+
     def run_layer(self, cache: ExpertCache, t: int, l: int, stream=None):
         s = self.shape
-        ft_moe_decode(cache.handle, l, self.x[t, l], self.ids[t, l], self.w[t, l], s.B, s.k,
-                      self.y[t, l], self.deferred[t, l], self.route_slot[t, l],
-                      self.counters[t, l], stream)
+        x, ids, w, y, d, rs, ct = self.addresses(t, l)
+        ft_moe_decode(cache.handle, l, x, ids, w, s.B, s.k, y, d, rs, ct, stream)
 
     def run_step(self, cache: ExpertCache, t: int, stream=None):
         for l in range(self.shape.L):
             self.run_layer(cache, t, l, stream)
+
+
+class StepGraph:
+    """One decode step (all L layer calls) captured as a CUDA graph over fixed
+    staging buffers; `replay(t)` copies step t's inputs in, replays, and copies the
+    outputs of the step back into the workload's arrays."""
+
+    def __init__(self, wl: DecodeWorkload, cache: ExpertCache):
+        self.wl, self.cache = wl, cache
+        self.x = wl.x[0].clone()
+        self.ids = wl.ids[0].clone()
+        self.w = wl.w[0].clone()
+        self.y = torch.empty_like(wl.y[0])
+        self.d = torch.empty_like(wl.deferred[0])
+        self.rs = torch.empty_like(wl.route_slot[0])
+        self.ct = torch.empty_like(wl.counters[0])
+        self.graph = None
+
+    def capture(self):
+        s = self.wl.shape
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        per = [(t.data_ptr(), t[0].numel() * t.element_size())
+               for t in (self.x, self.ids, self.w, self.y, self.d, self.rs, self.ct)]
+        with torch.cuda.graph(g, stream=side):
+            st = torch.cuda.current_stream().cuda_stream
+            for l in range(s.L):
+                x, ids, w, y, d, rs, ct = [b + l * n for b, n in per]
+                ft_moe_decode(self.cache.handle, l, x, ids, w, s.B, s.k, y, d, rs, ct, st)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = g
+
+    def replay(self, t: int):
+        wl = self.wl
+        self.x.copy_(wl.x[t], non_blocking=True)
+        self.ids.copy_(wl.ids[t], non_blocking=True)
+        self.w.copy_(wl.w[t], non_blocking=True)
+        self.graph.replay()
+        wl.y[t].copy_(self.y, non_blocking=True)
+        wl.deferred[t].copy_(self.d, non_blocking=True)
+        wl.route_slot[t].copy_(self.rs, non_blocking=True)
+        wl.counters[t].copy_(self.ct, non_blocking=True)
 
 
 def split_tuple(mode: str, f_q16: int = 65536):

@@ -222,8 +222,9 @@ ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t re
 
 /* Per-kernel device time accumulated while profiling is on (CUDA events around
  * each launch on the launching stream).  kind: 0 remap, 1 expert gate/up + fills,
- * 2 expert down + combine, 3 prefill GEMM1, 4 prefill GEMM2, 5 prefill other. */
-#define FT_PROF_KINDS 6
+ * 2 expert down + combine, 3 prefill GEMM1, 4 prefill GEMM2, 5 prefill other
+ * kernels, 6 prefill layer copies (on the cache's copy stream). */
+#define FT_PROF_KINDS 7
 ft_status ft_profile_enable(ft_cache* c, int32_t enable);
 ft_status ft_profile_read(ft_cache* c, double* total_ms /*[FT_PROF_KINDS]*/,
                           int64_t* launches /*[FT_PROF_KINDS]*/);
