@@ -380,9 +380,6 @@ def native_prefill(args, pool, b_p, hbm_gbs, world):
         chunk(flags)                                   # warm-up chunk
         torch.cuda.synchronize()
         barrier(world)
-        if name == "double_buffer":
-            ft.ft_profile_enable(cache.handle, True)
-            ft.ft_profile_read(cache.handle)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         for _ in range(args.prefill_chunks):
@@ -391,10 +388,16 @@ def native_prefill(args, pool, b_p, hbm_gbs, world):
         torch.cuda.synchronize()
         barrier(world)
         ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.prefill_chunks
-        if name == "double_buffer":
-            prof = ft.ft_profile_read(cache.handle)
-            ft.ft_profile_enable(cache.handle, False)
         res[name] = {"ms_per_chunk": ms, "tok_s": T * world / (ms / 1e3)}
+    # per-kernel breakdown from a separate chunk with CUDA events around every launch
+    # (events interleaved with the copy stream serialise it, so they stay out of the
+    # timed chunks above)
+    ft.ft_profile_enable(cache.handle, True)
+    ft.ft_profile_read(cache.handle)
+    chunk(0)
+    torch.cuda.synchronize()
+    prof = ft.ft_profile_read(cache.handle)
+    ft.ft_profile_enable(cache.handle, False)
     assert ft.ft_cache_status(cache.handle) == 0
     cache.close()
     link_ms = L * s.E * rec / (b_p * 1e9) * 1e3
@@ -421,7 +424,9 @@ def native_prefill(args, pool, b_p, hbm_gbs, world):
                  "gemm2_tflops": g2_flop / (g2_ms / g2_n / 1e3) / 1e12 if g2_n else None,
                  "gemm1_ms_per_layer": g1_ms / g1_n if g1_n else None,
                  "gemm2_ms_per_layer": g2_ms / g2_n if g2_n else None,
-                 "other_ms_per_layer": prof["prefill_other"][0] / max(g1_n, 1)},
+                 "other_ms_per_layer": prof["prefill_other"][0] / max(g1_n, 1),
+                 "copy_ms_per_layer": prof["prefill_copy"][0] / max(prof["prefill_copy"][1], 1),
+                 "profiled_chunk": "single-buffered, events around every launch and copy"},
     }
 
 
