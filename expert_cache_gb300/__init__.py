@@ -20,9 +20,8 @@ FT_OK, FT_ERR_ARG, FT_ERR_CUDA, FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, F
 FT_DEV_BAD_ID, FT_DEV_TIMEOUT = 0x1, 0x2
 FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR = 0, 1
 FT_PREFILL_DOUBLE_BUFFER = 1
-FT_PROF_KINDS = 7
-PROF_NAMES = ("remap", "gate_up", "down", "prefill_gemm1", "prefill_gemm2", "prefill_other",
-              "prefill_copy")
+FT_PROF_KINDS = 5
+PROF_NAMES = ("decode", "prefill_gemm1", "prefill_gemm2", "prefill_other", "prefill_copy")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() first")

@@ -26,12 +26,11 @@ WsLayout ws_layout(const ft_cache_desc& d) {
     w.usage = take((size_t)cmax * 8);
     w.lru_order = take((size_t)cmax * 4);
     w.scalars = take(sizeof(DevScalars));
-    w.units = take((R + 1) * sizeof(Unit));
-    w.route_pair = take(R * 4);
-    w.pair_tok = take(P * 4);
-    w.h = take(P * (size_t)d.I * 4);
-    w.o = take(P * (size_t)d.H * 4);
-    w.tile_done = take((size_t)(d.H / kDownRowsPerItem + 1) * 4);
+    w.sync = take(kSyncWords * 4);
+    w.h = take(P * (size_t)d.I * 8);
+    w.o = take(P * (size_t)d.H * 8);
+    w.hflag = take((R + 1) * (size_t)(d.I / decode_pairs(d.H)) * 8);
+    w.h_end = w.hflag + (R + 1) * (size_t)(d.I / decode_pairs(d.H)) * 8;
     if (d.T_max > 0) {
         // at least one 128-row tile so a TMA box never exceeds the sorted buffers
         const size_t RT = std::max<size_t>((size_t)d.T_max * d.k_max, 128);
@@ -84,8 +83,8 @@ static ft_status check_desc(const ft_cache_desc* d) {
     if (!d) return FT_ERR_ARG;
     const int cmax = d->capacity_max > 0 ? d->capacity_max : d->capacity;
     if (d->L < 1 || d->E < 1 || d->E > kMaxE) return FT_ERR_ARG;
-    if (d->H < 64 || d->H % 64 || d->H > 65536) return FT_ERR_ARG;
-    if (d->I < 32 || d->I % 32 || d->I > 65536) return FT_ERR_ARG;
+    if (d->H < 64 || d->H % 64 || d->H > kMaxH) return FT_ERR_ARG;
+    if (d->I < 32 || d->I % 32 || d->I > kMaxI) return FT_ERR_ARG;
     if (d->k_max < 1 || d->k_max > kMaxK || d->B_max < 1 || d->B_max > kMaxB) return FT_ERR_ARG;
     if (d->B_max * d->k_max > kMaxRoutes) return FT_ERR_ARG;
     if (d->capacity < 1 || d->capacity > kMaxC || cmax < d->capacity || cmax > kMaxC) return FT_ERR_ARG;
@@ -94,6 +93,45 @@ static ft_status check_desc(const ft_cache_desc* d) {
     if (d->split.mode == FT_SPLIT_QSTAR && (d->split.f_q16 < 1 || d->split.f_q16 > 65536)) return FT_ERR_ARG;
     return FT_OK;
 }
+
+namespace ft {
+
+// Arguments of a decode call except the per-call scratch (h, o, sync).
+DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids, const float* w,
+                       int B, int k, float* y, int32_t* deferred, int32_t* route_slot,
+                       int32_t* counters) {
+    uint8_t* ws = c->workspace;
+    DecodeArgs a{};
+    a.slot_for_id = reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id);
+    a.id_of_slot = reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot);
+    a.usage = reinterpret_cast<long long*>(ws + c->ws.usage);
+    a.lru_order = reinterpret_cast<int32_t*>(ws + c->ws.lru_order);
+    a.sc = reinterpret_cast<DevScalars*>(ws + c->ws.scalars);
+    a.host_pool = c->host_pool_dev;
+    a.slot_buf = c->slot_buf;
+    a.shared = static_cast<const uint8_t*>(c->d.shared_experts);
+    a.rec_bytes = c->rec.bytes;
+    a.off_gu_scales = c->rec.gu_scales;
+    a.off_d_codes = c->rec.d_codes;
+    a.off_d_scales = c->rec.d_scales;
+    a.off_s_gu = c->rec.s_gu;
+    a.off_s_d = c->rec.s_d;
+    a.L = c->d.L; a.E = c->d.E; a.H = c->d.H; a.I = c->d.I; a.C = c->C;
+    a.layer = layer; a.B = B; a.k = k;
+    a.R_cap = c->d.B_max * c->d.k_max;
+    a.split_mode = c->d.split.mode;
+    a.f_q16 = c->d.split.f_q16;
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.ids = ids;
+    a.w = w;
+    a.y = y;
+    a.deferred = deferred;
+    a.route_slot = route_slot;
+    a.counters = counters;
+    return a;
+}
+
+}  // namespace ft
 
 // TMA maps of the prefill GEMM operands (only when the cache supports prefill).
 static bool prefill_maps(ft_cache* c) {
@@ -167,7 +205,11 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
     c->prof = false;
     c->prof_n = 0;
     c->err[0] = 0;
-    c->grid_gemv = sm_count() * gemv_occupancy(d->H, d->I);
+    c->grid_decode = decode_grid(d->H, d->I, d->E, d->B_max * d->k_max);
+    if (c->grid_decode < 2) {
+        delete c;
+        return FT_ERR_CUDA;
+    }
 
     if ((e = cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking)) != cudaSuccess) {
         delete c;
@@ -185,6 +227,8 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
                            reinterpret_cast<long long*>(ws + c->ws.usage),
                            reinterpret_cast<int32_t*>(ws + c->ws.lru_order), c->C,
                            reinterpret_cast<DevScalars*>(ws + c->ws.scalars), true, c->copy_stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(ws + c->ws.sync, 0, c->ws.h_end - c->ws.sync, c->copy_stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->copy_stream);
     if (e != cudaSuccess) {
         ft_cache_destroy(c);
@@ -315,53 +359,18 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
     }
     c->buffer_layer[0] = c->buffer_layer[1] = -1;   // decode may evict prefill buffers
 
-    uint8_t* ws = c->workspace;
-    DecodeArgs a;
-    a.slot_for_id = reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id);
-    a.id_of_slot = reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot);
-    a.usage = reinterpret_cast<long long*>(ws + c->ws.usage);
-    a.lru_order = reinterpret_cast<int32_t*>(ws + c->ws.lru_order);
-    a.sc = reinterpret_cast<DevScalars*>(ws + c->ws.scalars);
-    a.units = reinterpret_cast<Unit*>(ws + c->ws.units);
-    a.route_pair = reinterpret_cast<int32_t*>(ws + c->ws.route_pair);
-    a.pair_tok = reinterpret_cast<int32_t*>(ws + c->ws.pair_tok);
-    a.h = reinterpret_cast<float*>(ws + c->ws.h);
-    a.o = reinterpret_cast<float*>(ws + c->ws.o);
-    a.tile_done = reinterpret_cast<unsigned*>(ws + c->ws.tile_done);
-    a.host_pool = c->host_pool_dev;
-    a.slot_buf = c->slot_buf;
-    a.shared = static_cast<const uint8_t*>(c->d.shared_experts);
-    a.rec_bytes = c->rec.bytes;
-    a.off_gu_scales = c->rec.gu_scales;
-    a.off_d_codes = c->rec.d_codes;
-    a.off_d_scales = c->rec.d_scales;
-    a.off_s_gu = c->rec.s_gu;
-    a.off_s_d = c->rec.s_d;
-    a.L = c->d.L; a.E = c->d.E; a.H = c->d.H; a.I = c->d.I; a.C = c->C;
-    a.layer = layer; a.B = B; a.k = k;
-    a.split_mode = c->d.split.mode;
-    a.f_q16 = c->d.split.f_q16;
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.ids = topk_ids;
-    a.w = topk_w;
-    a.y = y;
-    a.deferred = deferred;
-    a.route_slot = route_slot;
-    a.counters = counters;
-
-    cudaError_t e;
-    int p = prof_begin(c, 0, s);
-    e = launch_remap(a, s);
+    DecodeArgs a = decode_args(c, layer, x, topk_ids, topk_w, B, k, y, deferred, route_slot,
+                               counters);
+    a.h = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.h);
+    a.sync = reinterpret_cast<unsigned*>(c->workspace + c->ws.sync);
+    a.o = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.o);
+    a.hflag = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.hflag);
+    a.scrub = a.h;
+    a.scrub_words = (c->ws.h_end - c->ws.h) / 8;
+    const int p = prof_begin(c, 0, s);
+    const cudaError_t e = launch_decode(a, c->grid_decode, s);
     prof_end(c, p, s);
-    if (e != cudaSuccess) return cuda_fail(c, e, "remap launch");
-    p = prof_begin(c, 1, s);
-    e = launch_gate_up(a, c->grid_gemv, s);
-    prof_end(c, p, s);
-    if (e != cudaSuccess) return cuda_fail(c, e, "gate/up launch");
-    p = prof_begin(c, 2, s);
-    e = launch_down(a, c->grid_gemv, s);
-    prof_end(c, p, s);
-    if (e != cudaSuccess) return cuda_fail(c, e, "down launch");
+    if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
     return FT_OK;
 }
 
@@ -417,6 +426,9 @@ ft_status ft_cache_status(ft_cache* c, int32_t* device_status) {
     int* st = reinterpret_cast<int*>(c->workspace + c->ws.scalars + offsetof(DevScalars, status));
     if (e == cudaSuccess) e = cudaMemcpy(device_status, st, 4, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(st, 0, 4);
+    // a decode wait that ran out may have left its read counter non-zero
+    if (e == cudaSuccess && (*device_status & FT_DEV_TIMEOUT))
+        e = cudaMemset(c->workspace + c->ws.sync + 8, 0, 4);
     return e == cudaSuccess ? FT_OK : cuda_fail(c, e, "status");
 }
 

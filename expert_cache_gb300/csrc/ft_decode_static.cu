@@ -7,19 +7,20 @@
 // loop that must never enter the CUDA allocator (an allocation can synchronise the
 // device and stall the token pipeline).  Such a caller still owns the cache (its
 // tables live in the workspace given to ft_cache_create) and passes inputs and
-// outputs; only the per-call scratch (GPU unit list, route/token pair maps, the h
-// activations, the per-pair expert outputs and the row-tile counters) comes from
-// the static array below.
+// outputs; only the per-call scratch (the h activations, the per-pair expert
+// outputs and the grid state of the decode kernel) comes from the static array below.
 //
 // The array is a module-scope __device__ object: every GPU that loads this
 // library holds kStaticScratchBytes of it until the process exits.  In host code
 // its name is only a host-side stand-in, so the device address is looked up once
 // per device with cudaGetSymbolAddress, on the first call made on that device
 // (make that first call before any stream capture).  All calls share the array
-// and it keeps the last call's contents: the row-tile counters that must start at
-// zero are cleared by the remap kernel of every call, everything else is written
-// before it is read.  Calls that overlap on the GPU (two streams, two caches) race
-// on the array and must be serialised by the caller.
+// and it keeps the last call's contents: the decode kernel's grid state (a call
+// epoch shared by every cache that uses the array, and a counter that each call
+// returns to zero) starts zero-initialised when the module loads, and the h / o
+// words carry the epoch of the call that wrote them, so stale words are never
+// taken for fresh ones.  Calls that overlap on the GPU (two streams, two caches)
+// race on the array and must be serialised by the caller.
 #include <cstdio>
 #include <mutex>
 
@@ -69,15 +70,15 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     if (!x || !topk_ids || !topk_w || !y || !deferred) return fail(FT_ERR_ARG, "NULL argument");
     if (((uintptr_t)x) % 16) return fail(FT_ERR_ARG, "x must be 16-byte aligned");
 
-    // per-call scratch carve-up (same regions as the workspace's per-call part)
-    const size_t R = (size_t)B * k, P = R + B;
+    // per-call scratch carve-up: grid state first (same place for every cache
+    // shape), then the tagged h and o words
+    const size_t P = (size_t)B * k + B;
     size_t off = 0;
-    const size_t o_units = off;  off = up256(off + (R + 1) * sizeof(Unit));
-    const size_t o_rpair = off;  off = up256(off + R * 4);
-    const size_t o_ptok = off;   off = up256(off + P * 4);
-    const size_t o_h = off;      off = up256(off + P * (size_t)c->d.I * 4);
-    const size_t o_o = off;      off = up256(off + P * (size_t)c->d.H * 4);
-    const size_t o_tile = off;   off = up256(off + (size_t)(c->d.H / kDownRowsPerItem + 1) * 4);
+    const size_t o_sync = off;   off = up256(off + kSyncWords * 4);
+    const size_t o_h = off;      off = up256(off + P * (size_t)c->d.I * 8);
+    const size_t o_o = off;      off = up256(off + P * (size_t)c->d.H * 8);
+    const size_t U = (size_t)c->d.B_max * c->d.k_max + 1;
+    const size_t o_hf = off;     off = up256(off + U * (size_t)(c->d.I / decode_pairs(c->d.H)) * 8);
     if (off > kStaticScratchBytes)
         return fail(FT_ERR_ARG, "B, k, H and I need more than the 8 MiB static scratch");
     uint8_t* scr = scratch_address();
@@ -91,43 +92,15 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     }
     c->buffer_layer[0] = c->buffer_layer[1] = -1;
 
-    uint8_t* ws = c->workspace;
-    DecodeArgs a;
-    a.slot_for_id = reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id);
-    a.id_of_slot = reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot);
-    a.usage = reinterpret_cast<long long*>(ws + c->ws.usage);
-    a.lru_order = reinterpret_cast<int32_t*>(ws + c->ws.lru_order);
-    a.sc = reinterpret_cast<DevScalars*>(ws + c->ws.scalars);
-    a.units = reinterpret_cast<Unit*>(scr + o_units);
-    a.route_pair = reinterpret_cast<int32_t*>(scr + o_rpair);
-    a.pair_tok = reinterpret_cast<int32_t*>(scr + o_ptok);
-    a.h = reinterpret_cast<float*>(scr + o_h);
-    a.o = reinterpret_cast<float*>(scr + o_o);
-    a.tile_done = reinterpret_cast<unsigned*>(scr + o_tile);
-    a.host_pool = c->host_pool_dev;
-    a.slot_buf = c->slot_buf;
-    a.shared = static_cast<const uint8_t*>(c->d.shared_experts);
-    a.rec_bytes = c->rec.bytes;
-    a.off_gu_scales = c->rec.gu_scales;
-    a.off_d_codes = c->rec.d_codes;
-    a.off_d_scales = c->rec.d_scales;
-    a.off_s_gu = c->rec.s_gu;
-    a.off_s_d = c->rec.s_d;
-    a.L = c->d.L; a.E = c->d.E; a.H = c->d.H; a.I = c->d.I; a.C = c->C;
-    a.layer = layer; a.B = B; a.k = k;
-    a.split_mode = c->d.split.mode;
-    a.f_q16 = c->d.split.f_q16;
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.ids = topk_ids;
-    a.w = topk_w;
-    a.y = y;
-    a.deferred = deferred;
-    a.route_slot = route_slot;
-    a.counters = counters;
-
-    cudaError_t e = launch_remap(a, s);
-    if (e == cudaSuccess) e = launch_gate_up(a, c->grid_gemv, s);
-    if (e == cudaSuccess) e = launch_down(a, c->grid_gemv, s);
+    DecodeArgs a = decode_args(c, layer, x, topk_ids, topk_w, B, k, y, deferred, route_slot,
+                               counters);
+    a.h = reinterpret_cast<unsigned long long*>(scr + o_h);
+    a.sync = reinterpret_cast<unsigned*>(scr + o_sync);
+    a.o = reinterpret_cast<unsigned long long*>(scr + o_o);
+    a.hflag = reinterpret_cast<unsigned long long*>(scr + o_hf);
+    a.scrub = reinterpret_cast<unsigned long long*>(scr + o_h);
+    a.scrub_words = (kStaticScratchBytes - o_h) / 8;
+    const cudaError_t e = launch_decode(a, c->grid_decode, s);
     if (e != cudaSuccess) {
         snprintf(c->err, sizeof(c->err), "static decode launch: %s", cudaGetErrorString(e));
         return FT_ERR_CUDA;

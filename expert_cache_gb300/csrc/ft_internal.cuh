@@ -19,16 +19,35 @@ constexpr int kMaxE = 4096;            // experts per layer
 constexpr int kMaxC = 16384;           // slots
 constexpr int kMaxRoutes = 1023;       // B_max * k_max
 constexpr int kMaxB = 32;
+constexpr int kMaxH = 8192;            // hidden size (decode stages 4 tokens of x in smem)
+constexpr int kMaxI = 4096;            // intermediate size (4 tokens of h in smem)
 constexpr int kMaxK = 32;
 constexpr int kSlotsPerThread = kMaxC / kThreadsRemap;     // 16
 constexpr int kExpertsPerThread = kMaxE / kThreadsRemap;   // 4
 
-// Expert GEMV tiling.
-constexpr int kGemvThreads = 256;      // 8 warps
-constexpr int kRowPairsPerItem = 16;   // gate/up row pairs per gate-up work item
-constexpr int kDownRowsPerItem = 64;   // output rows per down work item
+// Decode layer kernel tiling.
+constexpr int kDecThreads = 256;       // 8 warps
 constexpr int kTokGroup = 4;           // tokens accumulated per pass
-constexpr int kCopyChunk = 32768;      // bytes per W_d copy work item of a fill
+
+// Work items of the decode kernel: a gate/up item holds decode_pairs(H) (gate row,
+// up row) pairs and a down item decode_rows(I) output rows, each at most 32 KB of
+// codes; both powers of two (so they divide I and H).
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int decode_pairs(int H) {
+    int p = 16;
+    while (p > 1 && p * H > 32768) p >>= 1;
+    return p;
+}
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int decode_rows(int I) {
+    int r = 64;
+    while (r > 8 && r * (I / 2) > 32768) r >>= 1;
+    return r;
+}
 
 // ----------------------------------------------------------------- record
 struct RecordLayout {
@@ -55,29 +74,14 @@ inline RecordLayout record_layout(int H, int I) {
 struct DevScalars {
     long long tick;        // one tick per decode / prefill layer call
     int status;            // FT_DEV_* bits
-    int n_units;           // GPU units of the current decode call (fills, hits, shared)
-    int n_fill;            // q
-    int n_hit;
-    int n_pairs;           // (unit, token) pairs
-    int shared_pair0;      // first pair of the shared unit, or -1
-    unsigned work1;        // gate/up work counter
-    unsigned work2;        // down work counter
-    int counters[4];       // n_hit, m, q, deferred routes
-    int pad[2];
-};
-
-// One expert computed on the GPU in a decode call.
-struct Unit {
-    const uint8_t* src;    // record to read: slot (hit), host pool (fill), shared
-    uint8_t* dst;          // slot to write while reading (fill), else nullptr
-    int pair0;             // first (unit, token) pair
-    int n_tok;             // number of tokens routed to this unit
+    int counters[4];       // last decode call: n_hit, m, q, deferred routes
+    int pad[3];
 };
 
 // Offsets of the workspace regions (bytes, 256-aligned).
 struct WsLayout {
     size_t slot_for_id, id_of_slot, usage, lru_order, scalars;
-    size_t units, route_pair, pair_tok, h, o, tile_done;
+    size_t sync, h, o, hflag, h_end;   // decode grid state; tagged words (h_end: end)
     // prefill region (present when T_max > 0)
     size_t pf_chunk_cnt, pf_offsets, pf_mtile, pf_perm, pf_route_pos;
     size_t pf_a_codes, pf_a_scales, pf_h_codes, pf_h_scales, pf_o;
@@ -86,25 +90,30 @@ struct WsLayout {
 
 WsLayout ws_layout(const ft_cache_desc& d);
 
-// Arguments of one decode call, passed by value to every decode kernel.
+// Grid state of the decode kernel (zero-initialised; see ft_decode.cu):
+// [epoch: 64-bit, words 0-1][read_done][unused]
+constexpr int kSyncWords = 4;
+
+// Arguments of one decode call, passed by value to the decode kernel.
 struct DecodeArgs {
     int32_t* slot_for_id;
     int32_t* id_of_slot;
     long long* usage;
     int32_t* lru_order;
     DevScalars* sc;
-    Unit* units;
-    int32_t* route_pair;
-    int32_t* pair_tok;
-    float* h;              // [n_pairs, I]
-    float* o;              // [n_pairs, H]
-    unsigned* tile_done;   // [H / kDownRowsPerItem]
+    unsigned long long* h; // [pairs, I] tagged values (tag << 32 | fp32 bits)
+    unsigned long long* o; // [pairs, H] tagged values
+    unsigned long long* hflag;  // [R_cap + 1, I / decode_pairs(H)] gate/up item done (tag)
+    unsigned* sync;        // kSyncWords words of grid state, 8-byte aligned
+    unsigned long long* scrub;  // the whole h / o region of this call's scratch ...
+    size_t scrub_words;         // ... in 8-byte words (periodic tag scrub)
     const uint8_t* host_pool;   // device-mapped address of the pinned pool
     uint8_t* slot_buf;
     const uint8_t* shared;      // device, or nullptr
     size_t rec_bytes;
     size_t off_gu_scales, off_d_codes, off_d_scales, off_s_gu, off_s_d;
     int L, E, H, I, C, layer, B, k;
+    int R_cap;             // B_max * k_max: sizes of the per-call arrays
     int split_mode;
     unsigned f_q16;
     const __nv_bfloat16* x;
@@ -120,14 +129,14 @@ struct DecodeArgs {
 cudaError_t launch_init_tables(int32_t* slot_for_id, int n_ids, int32_t* id_of_slot,
                                long long* usage, int32_t* lru_order, int C,
                                DevScalars* sc, bool reset_tick, cudaStream_t s);
-cudaError_t launch_remap(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_gate_up(const DecodeArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_down(const DecodeArgs& a, int grid, cudaStream_t s);
+// Grid of the decode kernel for a cache shape (every CTA resident at once), and the
+// launch; both take the cache's B_max * k_max as R_cap.
+int decode_grid(int H, int I, int E, int R_cap);
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s);
 
 int sm_count();
-int gemv_occupancy(int H, int I);
 
 // ----------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
@@ -208,7 +217,7 @@ struct ft_cache {
     CUtensorMap map_a1, map_b1;     // GEMM1: quantised x rows; W_gu codes of the slots
     CUtensorMap map_a2, map_b2;     // GEMM2: quantised h rows; W_d codes of the slots
     bool maps_ok;
-    int grid_gemv;
+    int grid_decode;
     // profiling
     bool prof;
     static constexpr int kProfEvents = 65536;
@@ -219,3 +228,10 @@ struct ft_cache {
     long long prof_launches[FT_PROF_KINDS];
     char err[256];
 };
+
+namespace ft {
+// Arguments of a decode call on cache c except the per-call scratch (h, o, sync).
+DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids, const float* w,
+                       int B, int k, float* y, int32_t* deferred, int32_t* route_slot,
+                       int32_t* counters);
+}  // namespace ft

@@ -52,7 +52,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
         cudaEvent_t e1 = nullptr;
         if (c->prof && c->prof_n * 2 + 2 <= ft_cache::kProfEvents) {
             const int i = c->prof_n++;
-            c->prof_kind[i] = 6;
+            c->prof_kind[i] = 4;
             cudaEventRecord(c->prof_ev[2 * i], c->copy_stream);
             e1 = c->prof_ev[2 * i + 1];
         }
@@ -130,7 +130,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
         return r;
     };
 
-    e = prof_kernel(5, [&] { return launch_pf_sort_quant(a, s); });
+    e = prof_kernel(3, [&] { return launch_pf_sort_quant(a, s); });
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "route sort launch");
 
     UmmaArgs g;
@@ -158,7 +158,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     g.off_b_scales = c->rec.gu_scales;
     g.off_tscale = c->rec.s_gu;
     g.a_scales = a.a_scales;
-    e = prof_kernel(3, [&] { return launch_umma(c->map_a1, c->map_b1, g, grid, s); });
+    e = prof_kernel(1, [&] { return launch_umma(c->map_a1, c->map_b1, g, grid, s); });
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "GEMM1 launch");
 
     g.kind = 2;
@@ -167,10 +167,10 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     g.off_b_scales = c->rec.d_scales;
     g.off_tscale = c->rec.s_d;
     g.a_scales = a.h_scales;
-    e = prof_kernel(4, [&] { return launch_umma(c->map_a2, c->map_b2, g, grid, s); });
+    e = prof_kernel(2, [&] { return launch_umma(c->map_a2, c->map_b2, g, grid, s); });
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "GEMM2 launch");
 
-    e = prof_kernel(5, [&] { return launch_pf_combine(a, s); });
+    e = prof_kernel(3, [&] { return launch_pf_combine(a, s); });
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "combine launch");
     cudaEventRecord(c->compute_done[b], s);
     return FT_OK;

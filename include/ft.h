@@ -72,8 +72,8 @@ typedef struct {
 typedef struct {
     int32_t L;              /* MoE layers */
     int32_t E;              /* routed experts per layer (1..4096) */
-    int32_t H;              /* hidden size, multiple of 64 */
-    int32_t I;              /* expert intermediate size, multiple of 32 */
+    int32_t H;              /* hidden size, multiple of 64, at most 8192 */
+    int32_t I;              /* expert intermediate size, multiple of 32, at most 4096 */
     int32_t k_max;          /* largest top-k passed to ft_moe_decode (1..32) */
     int32_t B_max;          /* largest decode batch (1..32) */
     int32_t capacity;       /* slots C at creation (1..16384) */
@@ -164,7 +164,7 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
  * call before any stream capture.  Every call shares the array: calls that
  * overlap on the GPU race and must be serialised by the caller.  Errors: those of
  * ft_moe_decode, and FT_ERR_ARG when B, k, H and I need more than 8 MiB of
- * scratch (about (B*k + B) * (H + I) * 4 bytes). */
+ * scratch (about (B*k + B) * (H + I) * 8 bytes). */
 ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t B,
                                int32_t k, float* y, int32_t* deferred, int32_t* route_slot,
@@ -221,10 +221,10 @@ ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t re
                          double* gbps);
 
 /* Per-kernel device time accumulated while profiling is on (CUDA events around
- * each launch on the launching stream).  kind: 0 remap, 1 expert gate/up + fills,
- * 2 expert down + combine, 3 prefill GEMM1, 4 prefill GEMM2, 5 prefill other
- * kernels, 6 prefill layer copies (on the cache's copy stream). */
-#define FT_PROF_KINDS 7
+ * each launch on the launching stream).  kind: 0 decode layer kernel, 1 prefill
+ * GEMM1, 2 prefill GEMM2, 3 prefill other kernels, 4 prefill layer copies (on the
+ * cache's copy stream). */
+#define FT_PROF_KINDS 5
 ft_status ft_profile_enable(ft_cache* c, int32_t enable);
 ft_status ft_profile_read(ft_cache* c, double* total_ms /*[FT_PROF_KINDS]*/,
                           int64_t* launches /*[FT_PROF_KINDS]*/);

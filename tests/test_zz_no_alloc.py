@@ -59,6 +59,7 @@ def test_static_scratch_decode_matches_workspace_decode(ft):
 
 def test_static_scratch_rejects_oversized_calls(ft):
     from expert_cache_gb300.workloads import build_pool
+    # (B*k + B) * (H + I) * 8 bytes of tagged h and o: 1024 pairs x 4128 x 8 B > 8 MiB
     L, E, H, I, k, B = 1, 4, 4096, 32, 31, 32
     pool = build_pool(12, L, E, H, I)
     cache = ft.ExpertCache(L, E, H, I, k, B, 4, pool.ptr)
