@@ -139,6 +139,11 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# From the ncu traffic capture of decode_layer_kernel (profiles/): DRAM bytes per
+# algorithmic HBM byte.
+DRAM_READ_PER_ALGORITHMIC_BYTE = 1.019
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -289,7 +294,13 @@ def native_decode(args, rank, world):
         "peak": eff_peak / 1e9,
         "unit": "GB/s",
         "frac": (per_launch / t_launch) / eff_peak,
-        "traffic": None,
+        # DRAM bytes per launch: the ncu capture of this kernel on the same layer shape over a
+        # small pool read 1.019 x the algorithmic HBM bytes (median over 16 launches), scaled
+        # here to this run's HBM bytes per launch; fills do not touch DRAM on the way in
+        "traffic": DRAM_READ_PER_ALGORITHMIC_BYTE * hbm_bytes / n_dec,
+        "traffic_note": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of decode_layer_kernel on "
+                         "workload qwen_decode_small (read = %.3f x algorithmic HBM bytes, write 0), "
+                         "scaled to this run's HBM bytes per launch" % DRAM_READ_PER_ALGORITHMIC_BYTE),
         "peak_note": (f"byte-mix peak of this kernel: HBM bytes at {hbm_gbs:.0f} GB/s ({peak_src} "
                       f"MEASURED_PEAKS hbm_gbs) plus host-link bytes at B_P = {b_p:.1f} GB/s "
                       "measured in this run; duration from CUDA events around each launch of an "
