@@ -139,37 +139,37 @@ __device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target) {
 
 
 
-// The 8 tagged words addr(0..7) (nullptr: no word), once each carries `tag`: every
+// The N tagged words addr(0..N-1) (nullptr: no word), once each carries `tag`: every
 // load of a round is in flight at once and only the stale words are reloaded
 // (bounded wait).
-template <typename AddrF>
-__device__ __forceinline__ void fetch_tagged8(AddrF addr, unsigned tag, float* out, int* timeout) {
+template <int N = 8, typename AddrF>
+__device__ __forceinline__ void fetch_tagged(AddrF addr, unsigned tag, float* out, int* timeout) {
     const unsigned long long ready = (unsigned long long)tag << 32;
-    unsigned long long raw[8];
+    unsigned long long raw[N];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < N; ++i) {
         const unsigned long long* p = addr(i);
         raw[i] = p ? ld_relaxed_u64(p) : ready;
     }
     bool ok = true;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ok &= (unsigned)(raw[i] >> 32) == tag;
+    for (int i = 0; i < N; ++i) ok &= (unsigned)(raw[i] >> 32) == tag;
     if (!ok) {
         const unsigned long long t0 = gtime();
         for (unsigned it = 0; it < kWaitIters && !ok; ++it) {
             __nanosleep(64);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < N; ++i)
                 if ((unsigned)(raw[i] >> 32) != tag) raw[i] = ld_relaxed_u64(addr(i));
             ok = true;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ok &= (unsigned)(raw[i] >> 32) == tag;
+            for (int i = 0; i < N; ++i) ok &= (unsigned)(raw[i] >> 32) == tag;
             if (!ok && (it & 63u) == 63u && gtime() - t0 > kWaitNs) break;
         }
         if (!ok) *timeout = 1;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out[i] = __uint_as_float((unsigned)raw[i]);
+    for (int i = 0; i < N; ++i) out[i] = __uint_as_float((unsigned)raw[i]);
 }
 
 // ------------------------------------------------------------------ arithmetic helpers
@@ -766,7 +766,7 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, float* hs, uint8_t
         const unsigned long long* f = a.hflag + (size_t)u * T1;
         for (int j0 = threadIdx.x; j0 < T1; j0 += 8 * 32) {
             float unused[8];
-            fetch_tagged8([&](int i) { return j0 + i * 32 < T1 ? f + j0 + i * 32 : nullptr; }, tag,
+            fetch_tagged<8>([&](int i) { return j0 + i * 32 < T1 ? f + j0 + i * 32 : nullptr; }, tag,
                           unused, &timeout);
         }
     }
@@ -783,7 +783,7 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, float* hs, uint8_t
         for (int e0 = threadIdx.x; e0 < ne; e0 += 8 * kThreads) {
             float v[8];
             const unsigned long long* hb = a.h + (size_t)(pair0 + g0) * I + e0;
-            fetch_tagged8([&](int i) { return e0 + i * kThreads < ne ? hb + i * kThreads : nullptr; },
+            fetch_tagged<8>([&](int i) { return e0 + i * kThreads < ne ? hb + i * kThreads : nullptr; },
                           tag, v, &timeout);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -807,7 +807,7 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, float* hs, uint8_t
 }
 
 // y rows of down item rt for every token: sum_j w[b,j] o_(b,j) in order j, + shared.
-// The o words of a (token, row) are fetched 8 at a time (all in flight at once).
+// The o words of a (token, row) are fetched 16 at a time (all in flight at once).
 __device__ void combine_tile(const DecodeArgs& a, SmemStatic& S, const Decision& D, int rt,
                              int pair0_shared) {
     const int H = a.H, B = a.B, k = a.k, R = decode_rows(a.I);
@@ -822,14 +822,14 @@ __device__ void combine_tile(const DecodeArgs& a, SmemStatic& S, const Decision&
             return j < k ? D.r_pair[b * k + j] : (j < nterm ? pair0_shared + b : -1);
         };
         float v = 0.f;
-        for (int j0 = 0; j0 < nterm; j0 += 8) {
-            float ov[8];
-            fetch_tagged8([&](int i) -> const unsigned long long* {
+        for (int j0 = 0; j0 < nterm; j0 += 16) {
+            float ov[16];
+            fetch_tagged<16>([&](int i) -> const unsigned long long* {
                 const int pj = j0 + i < nterm ? pair_of(j0 + i) : -1;
                 return pj >= 0 ? a.o + (size_t)pj * H + rr : nullptr;
             }, tag, ov, &timeout);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 const int j = j0 + i;
                 if (j >= nterm || pair_of(j) < 0) continue;
                 v = j < k ? fmaf(a.w[b * k + j], ov[i], v) : v + ov[i];
