@@ -28,9 +28,9 @@ WsLayout ws_layout(const ft_cache_desc& d) {
     w.scalars = take(sizeof(DevScalars));
     w.sync = take(kSyncWords * 4);
     w.h = take(P * (size_t)d.I * 8);
-    w.o = take(P * (size_t)d.H * 8);
     w.hflag = take((R + 1) * (size_t)(d.I / decode_pairs(d.H)) * 8);
-    w.h_end = w.hflag + (R + 1) * (size_t)(d.I / decode_pairs(d.H)) * 8;
+    w.yflag = take((size_t)(d.H / decode_rows(d.I)) * 8);
+    w.h_end = w.yflag + (size_t)(d.H / decode_rows(d.I)) * 8;
     if (d.T_max > 0) {
         // at least one 128-row tile so a TMA box never exceeds the sorted buffers
         const size_t RT = std::max<size_t>((size_t)d.T_max * d.k_max, 128);
@@ -363,8 +363,8 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
                                counters);
     a.h = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.h);
     a.sync = reinterpret_cast<unsigned*>(c->workspace + c->ws.sync);
-    a.o = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.o);
     a.hflag = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.hflag);
+    a.yflag = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.yflag);
     a.scrub = a.h;
     a.scrub_words = (c->ws.h_end - c->ws.h) / 8;
     const int p = prof_begin(c, 0, s);

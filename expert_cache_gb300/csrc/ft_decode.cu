@@ -124,6 +124,19 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
 __device__ __forceinline__ unsigned long long tagged(float v, unsigned tag) {
     return ((unsigned long long)tag << 32) | __float_as_uint(v);
 }
+// Release store / acquire load of a tagged word (a flag that orders other data).
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// y += v (fp32 add performed at the L2; the order of the adds to one word is free).
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+}
 
 // One thread waits until *p >= target; false when the bound ran out.
 __device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target) {
@@ -137,7 +150,18 @@ __device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target) {
     return false;
 }
 
-
+// One thread waits until the tagged word *p carries `tag` (acquire); false when the
+// bound ran out.
+__device__ __forceinline__ bool wait_tag_acquire(const unsigned long long* p, unsigned tag) {
+    if ((unsigned)(ld_acquire_u64(p) >> 32) == tag) return true;
+    const unsigned long long t0 = gtime();
+    for (unsigned it = 0; it < kWaitIters; ++it) {
+        __nanosleep(64);
+        if ((unsigned)(ld_acquire_u64(p) >> 32) == tag) return true;
+        if ((it & 63u) == 63u && gtime() - t0 > kWaitNs) break;
+    }
+    return false;
+}
 
 // The N tagged words addr(0..N-1) (nullptr: no word), once each carries `tag`: every
 // load of a round is in flight at once and only the stale words are reloaded
@@ -307,6 +331,7 @@ struct SmemStatic {
     int tpre[kMaxC / 32 + 1];
     int scan[33];
     float xmul[kTok];
+    float uw[kMaxB];            // routing weights of the current down item's tokens
     float red[kTok][kWarps];
     // the decision's scalars
     int n_hit, m, q, n_routed, n_units, n_pairs, n_def, bad;
@@ -524,6 +549,26 @@ __device__ __forceinline__ void stage_block(const uint8_t* src, uint8_t* dst, ui
     }
 }
 
+// A fill item's share of the record: up to four runs, each (source in the pinned
+// pool, destination in the victim slot, destination in shared memory, 16-byte pieces).
+struct FillRuns {
+    const uint8_t* src[4];
+    uint8_t* dst[4];
+    uint8_t* sm[4];
+    int n16[4];                 // 0: run unused
+};
+
+// Stages a fill item through registers, run after run (each run coalesced and
+// contiguous; several runs in flight at once read the host link less efficiently
+// once two or more fills share it).  Each piece goes to shared memory and into the
+// victim slot on the way; the pieces are in shared memory after the caller's next
+// barrier.  Out of line, so that its registers do not add to the kernel's hot loops.
+__device__ __noinline__ void stage_fill(const FillRuns& fr) {
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r)
+        if (fr.n16[r] > 0) stage_block(fr.src[r], fr.dst[r], fr.sm[r], (uint32_t)fr.n16[r] * 16, nullptr);
+}
+
 // Arms `bar` for `bytes` of bulk copies (thread 0; hits and the shared expert only).
 __device__ __forceinline__ void arm_bulk(uint64_t* bar, uint32_t bytes) {
     if (threadIdx.x == 0) {
@@ -544,11 +589,19 @@ __device__ __forceinline__ void stage_gate_up(const DecodeArgs& a, UnitRef ur, i
     const size_t su = a.off_gu_scales + (size_t)(I + tile * P) * (H / 16);
     const uint32_t nc = (uint32_t)P * (H / 2), ns = (uint32_t)P * (H / 16);
     uint8_t* d = ur.dst;
-    if (d == nullptr) arm_bulk(bar, 2 * (nc + ns));
-    stage_block(ur.src + cg, d ? d + cg : nullptr, wc, nc, bar);
-    stage_block(ur.src + cu, d ? d + cu : nullptr, wc + nc, nc, bar);
-    stage_block(ur.src + sg, d ? d + sg : nullptr, ws, ns, bar);
-    stage_block(ur.src + su, d ? d + su : nullptr, ws + ns, ns, bar);
+    if (d == nullptr) {
+        arm_bulk(bar, 2 * (nc + ns));
+        stage_block(ur.src + cg, nullptr, wc, nc, bar);
+        stage_block(ur.src + cu, nullptr, wc + nc, nc, bar);
+        stage_block(ur.src + sg, nullptr, ws, ns, bar);
+        stage_block(ur.src + su, nullptr, ws + ns, ns, bar);
+        return;
+    }
+    const FillRuns fr{{ur.src + cg, ur.src + cu, ur.src + sg, ur.src + su},
+                      {d + cg, d + cu, d + sg, d + su},
+                      {wc, wc + nc, ws, ws + ns},
+                      {(int)nc / 16, (int)nc / 16, (int)ns / 16, (int)ns / 16}};
+    stage_fill(fr);
 }
 
 // h = silu(g) * u of the item's row pairs for NT tokens (x rows xrow[]), from the
@@ -676,20 +729,30 @@ __device__ __forceinline__ void stage_down(const DecodeArgs& a, UnitRef ur, int 
     const size_t so = a.off_d_scales + (size_t)(rt * R) * (I / 16);
     const uint32_t nc = (uint32_t)R * (I / 2), ns = (uint32_t)R * (I / 16);
     uint8_t* d = ur.dst;
-    if (d == nullptr) arm_bulk(bar, nc + ns);
-    stage_block(ur.src + co, d ? d + co : nullptr, dc, nc, bar);
-    stage_block(ur.src + so, d ? d + so : nullptr, ds, ns, bar);
-    if (d != nullptr && rt == 0 && threadIdx.x < 2)     // tensor scales s_gu, s_d of the fill
+    if (d == nullptr) {
+        arm_bulk(bar, nc + ns);
+        stage_block(ur.src + co, nullptr, dc, nc, bar);
+        stage_block(ur.src + so, nullptr, ds, ns, bar);
+        return;
+    }
+    const FillRuns fr{{ur.src + co, ur.src + so, nullptr, nullptr},
+                      {d + co, d + so, nullptr, nullptr},
+                      {dc, ds, nullptr, nullptr},
+                      {(int)nc / 16, (int)ns / 16, 0, 0}};
+    stage_fill(fr);
+    if (rt == 0 && threadIdx.x < 2)     // tensor scales s_gu, s_d of the fill
         reinterpret_cast<float*>(d + a.off_s_gu)[threadIdx.x] =
             reinterpret_cast<const float*>(ur.src + a.off_s_gu)[threadIdx.x];
 }
 
-// o = s_d * W_d h for the item's rows and NT tokens, from the staged weights.
+// o = s_d * W_d h for the item's rows and NT tokens (the set bits g0 .. g0+NT-1 of
+// the unit's token mask, routing weights S.uw[g0 + t]), from the staged weights,
+// added into y: y[token, row] += weight * o.
 // Warp w takes rows R/8 * w .. +R/8-1; a row is read by lpr lanes (the power of
 // two >= its 16-byte chunks, at most 32), so one instruction covers 32/lpr rows.
 template <int NT>
 __device__ void down_rows(const DecodeArgs& a, const SmemStatic& S, const float* hs, const uint8_t* dc,
-                          const uint8_t* ds, int rt, int pair0, float s_d) {
+                          const uint8_t* ds, int rt, uint32_t tokmask, int g0, float s_d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, R = decode_rows(I);
     const int nch = I / 32, rb = I / 2, srow = I / 16, hpieces = I / 4;
@@ -743,22 +806,36 @@ __device__ void down_rows(const DecodeArgs& a, const SmemStatic& S, const float*
         for (int t = 0; t < NT; ++t) {
             float v = acc[t];
             for (int o = lpr >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (li == 0 && rok)
-                st_relaxed_u64(a.o + (size_t)(pair0 + t) * H + rt * R + rl, tagged(v * s_d, S.tag));
+            if (li == 0 && rok) {
+                const int tok = (int)__fns(tokmask, 0, g0 + t + 1);
+                red_add_f32(a.y + (size_t)tok * H + rt * R + rl, S.uw[g0 + t] * (v * s_d));
+            }
         }
     }
 }
 
 // One down item: stage the weights (unless prefetched), wait for the unit's h,
-// then every token group.
-__device__ void down_item(const DecodeArgs& a, SmemStatic& S, float* hs, uint8_t* dc, uint8_t* ds,
-                          uint32_t& par_d, bool prefetched, UnitRef ur, int u, int rt, int pair0,
-                          uint32_t tokmask) {
+// then every token group, added into y.  A token's weight for a routed unit is the
+// sum of its routing weights to that expert (one route, unless the token lists the
+// expert twice); for the shared expert it is 1.
+__device__ void down_item(const DecodeArgs& a, SmemStatic& S, const Decision& D, float* hs, uint8_t* dc,
+                          uint8_t* ds, uint32_t& par_d, bool prefetched, UnitRef ur, int u, bool shared_unit,
+                          int rt, int pair0, uint32_t tokmask) {
     const int I = a.I;
     const bool fill = ur.dst != nullptr;
     const unsigned tag = S.tag;
     const float s_d = *reinterpret_cast<const float*>(ur.src + a.off_s_d);
     if (!prefetched) stage_down(a, ur, rt, dc, ds, &S.bar_d);
+    if ((int)threadIdx.x < __popc(tokmask)) {          // (published by the barrier below)
+        const int b = (int)__fns(tokmask, 0, threadIdx.x + 1);
+        float wsum = 1.f;
+        if (!shared_unit) {
+            wsum = 0.f;
+            for (int j = 0; j < a.k; ++j)
+                if (D.r_unit[b * a.k + j] == u) wsum += a.w[b * a.k + j];
+        }
+        S.uw[threadIdx.x] = wsum;
+    }
     int timeout = 0;
     // the unit's gate/up items have all raised their flags ...
     const int T1 = I / decode_pairs(a.H);
@@ -796,46 +873,12 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, float* hs, uint8_t
         }
         __syncthreads();                                   // h (and the fills' weights) visible
         switch (ntg) {
-            case 1: down_rows<1>(a, S, hs, dc, ds, rt, pair0 + g0, s_d); break;
-            case 2: down_rows<2>(a, S, hs, dc, ds, rt, pair0 + g0, s_d); break;
-            case 3: down_rows<3>(a, S, hs, dc, ds, rt, pair0 + g0, s_d); break;
-            default: down_rows<4>(a, S, hs, dc, ds, rt, pair0 + g0, s_d); break;
+            case 1: down_rows<1>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
+            case 2: down_rows<2>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
+            case 3: down_rows<3>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
+            default: down_rows<4>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
         }
         __syncthreads();                                   // hs is restaged by the next group
-    }
-    if (timeout) S.timeout = 1;
-}
-
-// y rows of down item rt for every token: sum_j w[b,j] o_(b,j) in order j, + shared.
-// The o words of a (token, row) are fetched 16 at a time (all in flight at once).
-__device__ void combine_tile(const DecodeArgs& a, SmemStatic& S, const Decision& D, int rt,
-                             int pair0_shared) {
-    const int H = a.H, B = a.B, k = a.k, R = decode_rows(a.I);
-    const unsigned tag = S.tag;
-    const int nterm = k + (pair0_shared >= 0 ? 1 : 0);
-    int timeout = 0;
-    for (int idx = threadIdx.x; idx < B * R; idx += kThreads) {
-        const int b = idx / R;
-        const int rr = rt * R + idx % R;
-        // term j < k: route j (skipped when not on the GPU); term k: the shared expert
-        auto pair_of = [&](int j) {
-            return j < k ? D.r_pair[b * k + j] : (j < nterm ? pair0_shared + b : -1);
-        };
-        float v = 0.f;
-        for (int j0 = 0; j0 < nterm; j0 += 16) {
-            float ov[16];
-            fetch_tagged<16>([&](int i) -> const unsigned long long* {
-                const int pj = j0 + i < nterm ? pair_of(j0 + i) : -1;
-                return pj >= 0 ? a.o + (size_t)pj * H + rr : nullptr;
-            }, tag, ov, &timeout);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j = j0 + i;
-                if (j >= nterm || pair_of(j) < 0) continue;
-                v = j < k ? fmaf(a.w[b * k + j], ov[i], v) : v + ov[i];
-            }
-        }
-        a.y[(size_t)b * H + rr] = v;
     }
     if (timeout) S.timeout = 1;
 }
@@ -1241,11 +1284,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         // ---- every 2^31 calls: zero the scratch words this call does not use
         if ((S.tag & 0x7fffffffu) == 1u) {
             const unsigned long long* h_end = a.h + (size_t)S.n_pairs * a.I;
-            const unsigned long long* o_end = a.o + (size_t)S.n_pairs * a.H;
             const unsigned long long* hf_end = a.hflag + (size_t)n_units * (a.I / decode_pairs(a.H));
+            const unsigned long long* yf_end = a.yflag + (n_units > 0 ? a.H / decode_rows(a.I) : 0);
             for (size_t i = tid; i < a.scrub_words; i += kThreads) {
                 unsigned long long* w = a.scrub + i;
-                const bool used = (w >= a.h && w < h_end) || (w >= a.o && w < o_end) ||
+                const bool used = (w >= a.h && w < h_end) || (w >= a.yflag && w < yf_end) ||
                                   (w >= a.hflag && w < hf_end);
                 if (!used) *w = 0ull;
             }
@@ -1260,8 +1303,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         return;
     }
     const int T1 = a.I / decode_pairs(a.H);              // gate/up items per unit
-    const int T2 = a.H / decode_rows(a.I);               // down items per unit
+    const int T2 = a.H / decode_rows(a.I);               // down items per unit (= row tiles)
     const int n1 = n_units * T1, n2 = n_units * T2;
+    // ---- y row tiles z == this CTA (mod n_compute): zeroed, then flagged (release)
+    // for the down items that add into them.  Warps 1..7 only: warp 0 issues the
+    // first weight copies meanwhile.
+    if (warp > 0) {
+        const int RW = decode_rows(a.I);
+        for (int z = blockIdx.x; z < T2; z += n_compute)
+            for (int i = tid - 32; i < B * RW; i += kThreads - 32)
+                a.y[(size_t)(i / RW) * a.H + z * RW + i % RW] = 0.f;
+        asm volatile("bar.sync 1, %0;" :: "r"(kThreads - 32) : "memory");
+        if (tid == 32)
+            for (int z = blockIdx.x; z < T2; z += n_compute) st_release_u64(a.yflag + z, tagged(0.f, S.tag));
+    }
     uint8_t* wc = dsm + L.wc;
     uint8_t* ws = dsm + L.ws;
     uint8_t* dc = dsm + L.dc;
@@ -1284,19 +1339,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         if (tid == 0) st_relaxed_u64(a.hflag + (size_t)u * T1 + tile, tagged(0.f, S.tag));
     }
     if (prefetch_due) prefetch_down(a, D, q, n_routed, p_first / T2, p_first % T2, dc, ds, &S.bar_d);
+    // the y tiles of this CTA's down items are zeroed (acquire: the adds come after)
+    if (warp == 0) {
+        int timeout = 0;
+        for (int p = p_first + lane * n_compute; p < n2; p += 32 * n_compute)
+            if (!wait_tag_acquire(a.yflag + p % T2, S.tag)) timeout = 1;
+        if (timeout) S.timeout = 1;
+    }
     float* hs = reinterpret_cast<float*>(dsm + L.stage);
     for (int p = p_first; p < n2; p += n_compute) {
         const int u = p / T2, rt = p % T2;
-        down_item(a, S, hs, dc, ds, par_d, prefetch && p == p_first, unit_ref_of(a, D, q, n_routed, u), u, rt,
-                  D.u_pair0[u], D.u_mask[u]);
+        down_item(a, S, D, hs, dc, ds, par_d, prefetch && p == p_first, unit_ref_of(a, D, q, n_routed, u), u,
+                  u >= n_routed, rt, D.u_pair0[u], D.u_mask[u]);
     }
-    // ---- the row tiles whose last unit this CTA computed
-    const int pair0_shared = n_units > n_routed ? D.u_pair0[n_routed] : -1;
-    for (int p = p_first; p < n2; p += n_compute)
-        if (p / T2 == n_units - 1) {
-            combine_tile(a, S, D, p % T2, pair0_shared);
-            __syncthreads();
-        }
     if (tid == 0 && S.timeout) atomicOr(&a.sc->status, FT_DEV_TIMEOUT);
 }
 

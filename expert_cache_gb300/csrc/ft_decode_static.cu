@@ -7,8 +7,8 @@
 // loop that must never enter the CUDA allocator (an allocation can synchronise the
 // device and stall the token pipeline).  Such a caller still owns the cache (its
 // tables live in the workspace given to ft_cache_create) and passes inputs and
-// outputs; only the per-call scratch (the h activations, the per-pair expert
-// outputs and the grid state of the decode kernel) comes from the static array below.
+// outputs; only the per-call scratch (the h activations, the per-item and per-tile
+// flags and the grid state of the decode kernel) comes from the static array below.
 //
 // The array is a module-scope __device__ object: every GPU that loads this
 // library holds kStaticScratchBytes of it until the process exits.  In host code
@@ -17,9 +17,9 @@
 // (make that first call before any stream capture).  All calls share the array
 // and it keeps the last call's contents: the decode kernel's grid state (a call
 // epoch shared by every cache that uses the array, and a counter that each call
-// returns to zero) starts zero-initialised when the module loads, and the h / o
-// words carry the epoch of the call that wrote them, so stale words are never
-// taken for fresh ones.  Calls that overlap on the GPU (two streams, two caches)
+// returns to zero) starts zero-initialised when the module loads, and the h words
+// and the flags carry the epoch of the call that wrote them, so stale words are
+// never taken for fresh ones.  Calls that overlap on the GPU (two streams, two caches)
 // race on the array and must be serialised by the caller.
 #include <cstdio>
 #include <mutex>
@@ -71,16 +71,16 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     if (((uintptr_t)x) % 16) return fail(FT_ERR_ARG, "x must be 16-byte aligned");
 
     // per-call scratch carve-up: grid state first (same place for every cache
-    // shape), then the tagged h and o words
+    // shape), then the tagged h words and flags
     const size_t P = (size_t)B * k + B;
     size_t off = 0;
     const size_t o_sync = off;   off = up256(off + kSyncWords * 4);
     const size_t o_h = off;      off = up256(off + P * (size_t)c->d.I * 8);
-    const size_t o_o = off;      off = up256(off + P * (size_t)c->d.H * 8);
     const size_t U = (size_t)c->d.B_max * c->d.k_max + 1;
     const size_t o_hf = off;     off = up256(off + U * (size_t)(c->d.I / decode_pairs(c->d.H)) * 8);
+    const size_t o_yf = off;     off = up256(off + (size_t)(c->d.H / decode_rows(c->d.I)) * 8);
     if (off > kStaticScratchBytes)
-        return fail(FT_ERR_ARG, "B, k, H and I need more than the 8 MiB static scratch");
+        return fail(FT_ERR_ARG, "B, k and I need more than the 8 MiB static scratch");
     uint8_t* scr = scratch_address();
     if (!scr) return fail(FT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
 
@@ -96,8 +96,8 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
                                counters);
     a.h = reinterpret_cast<unsigned long long*>(scr + o_h);
     a.sync = reinterpret_cast<unsigned*>(scr + o_sync);
-    a.o = reinterpret_cast<unsigned long long*>(scr + o_o);
     a.hflag = reinterpret_cast<unsigned long long*>(scr + o_hf);
+    a.yflag = reinterpret_cast<unsigned long long*>(scr + o_yf);
     a.scrub = reinterpret_cast<unsigned long long*>(scr + o_h);
     a.scrub_words = (kStaticScratchBytes - o_h) / 8;
     const cudaError_t e = launch_decode(a, c->grid_decode, s);

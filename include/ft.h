@@ -135,7 +135,8 @@ uint32_t  ft_split_from_overlap(double p_ov, double c_ov);
  *   5. the q fills are read from the pinned pool once, written into their slots and
  *      computed on the way (load-through over the host link);
  *   6. NVFP4 SwiGLU per unique GPU expert (hits + fills, + the shared expert);
- *   7. y[b] = sum_j w[b,j] * o_(b,j) over GPU routes in order j, + shared(x_b).
+ *   7. y[b] = sum_j w[b,j] * o_(b,j) over GPU routes, + shared(x_b); the terms are
+ *      fp32 adds in no fixed order, so y can differ between calls in the last bits.
  * Arguments:
  *   x          device bf16 [B, H]
  *   topk_ids   device int32 [B, k], local expert ids; an id outside [0, E) masks the
@@ -163,8 +164,8 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
  * address is looked up on the first call made on each device, so make that first
  * call before any stream capture.  Every call shares the array: calls that
  * overlap on the GPU race and must be serialised by the caller.  Errors: those of
- * ft_moe_decode, and FT_ERR_ARG when B, k, H and I need more than 8 MiB of
- * scratch (about (B*k + B) * (H + I) * 8 bytes). */
+ * ft_moe_decode, and FT_ERR_ARG when B, k and I need more than 8 MiB of scratch
+ * (about (B*k + B) * I * 8 bytes). */
 ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t B,
                                int32_t k, float* y, int32_t* deferred, int32_t* route_slot,

@@ -59,8 +59,8 @@ def test_static_scratch_decode_matches_workspace_decode(ft):
 
 def test_static_scratch_rejects_oversized_calls(ft):
     from expert_cache_gb300.workloads import build_pool
-    # (B*k + B) * (H + I) * 8 bytes of tagged h and o: 1024 pairs x 4128 x 8 B > 8 MiB
-    L, E, H, I, k, B = 1, 4, 4096, 32, 31, 32
+    # (B*k + B) * I * 8 bytes of tagged h: 1024 pairs x 2048 x 8 B = 16 MiB > 8 MiB
+    L, E, H, I, k, B = 1, 4, 4096, 2048, 31, 32
     pool = build_pool(12, L, E, H, I)
     cache = ft.ExpertCache(L, E, H, I, k, B, 4, pool.ptr)
     ids = torch.zeros((B, k), dtype=torch.int32, device="cuda")
