@@ -141,7 +141,7 @@ def peaks():
 
 # From the ncu traffic capture of decode_layer_kernel (profiles/): DRAM bytes per
 # algorithmic HBM byte.
-DRAM_READ_PER_ALGORITHMIC_BYTE = 1.019
+DRAM_READ_PER_ALGORITHMIC_BYTE = 1.011
 
 
 def cpu_cores():
@@ -295,7 +295,7 @@ def native_decode(args, rank, world):
         "unit": "GB/s",
         "frac": (per_launch / t_launch) / eff_peak,
         # DRAM bytes per launch: the ncu capture of this kernel on the same layer shape over a
-        # small pool read 1.019 x the algorithmic HBM bytes (median over 16 launches), scaled
+        # small pool read 1.011 x the algorithmic HBM bytes (median over 16 launches), scaled
         # here to this run's HBM bytes per launch; fills do not touch DRAM on the way in
         "traffic": DRAM_READ_PER_ALGORITHMIC_BYTE * hbm_bytes / n_dec,
         "traffic_note": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of decode_layer_kernel on "
