@@ -27,14 +27,17 @@
 //     reads the rows from the pinned pool over the host link and writes them into
 //     the victim slot on the way (one link read per byte).  Warp w then computes
 //     pairs w, w + 8, ... in rolled loops (the per-item code stays small enough
-//     for the instruction cache).
+//     for the instruction cache).  Meanwhile warps 1..7 of compute CTA z zero y's
+//     R-row tile z (mod the compute CTAs) and raise the tile's flag (release).
 //  3. Down items (unit, R output rows; R * I/2 <= 32 KB) go to CTAs G-2, G-3, ... so
 //     the fills' down items land on CTAs without gate/up work and fetch their W_d
 //     rows at once; a CTA's first down item of a hit unit is staged under its
-//     gate/up work.  Each waits for its unit's h and writes o = s_d W_d h (tagged).
-//  4. The CTA that ran the last unit's down item of a row tile sums, after all of
-//     its own items, y[b] = sum_j w[b,j] o_(b,j) in order j, then + shared.
-//  5. CTA G-1 writes the per-call outputs, waits until every compute CTA has read
+//     gate/up work.  A CTA first acquires the flags of its down items' y tiles;
+//     each item waits for its unit's h and adds w * s_d W_d h into y (fp32 adds at
+//     the L2; w = the token's routing weight to that expert, 1 for the shared
+//     expert).  That is the gated combine y[b] = sum_j w[b,j] o_(b,j) + shared,
+//     summed in arrival order; y is complete when the grid ends.
+//  4. CTA G-1 writes the per-call outputs, waits until every compute CTA has read
 //     the tables, then applies the update: fills mapped, evicted ids unmapped,
 //     touched slots stamped with the tick, LRU order rebuilt (untouched slots keep
 //     their order, touched ones follow in ascending slot order).
@@ -43,12 +46,13 @@
 // free slots (usage -1) first; the q victims are the first q entries that no hit
 // of this call holds, all within its first B*k positions.
 //
-// Exchange inside the grid: h and o values travel as single 64-bit words
-// (call tag << 32 | fp32 bits), stored and loaded with relaxed gpu-scope
-// accesses.  Each gate/up item raises a flag word (the tag) after a CTA barrier; a
-// down item has one warp wait for its unit's flags, then reads h, re-polling any
-// word whose store has not landed yet; a combine polls its o words directly.  Loads
-// go out 8 at a time.  No fence or counter sits between producer and consumer.  The tag is the
+// Exchange inside the grid: h values travel as single 64-bit words (call tag << 32
+// | fp32 bits), stored and loaded with relaxed gpu-scope accesses.  Each gate/up
+// item raises a flag word (the tag) after a CTA barrier; a down item has one warp
+// wait for its unit's flags, then reads h, re-polling any word whose store has not
+// landed yet.  Loads go out 8 at a time.  No fence or counter sits between those
+// producers and consumers; the y tile flags (zeroed data in other words) are the one
+// release / acquire pair.  The tag is the
 // low half of a 64-bit call epoch kept in the scratch (never 0); every 2^31 calls
 // the commit CTA zeroes the scratch words this call does not use, so no word is
 // older than 2^31 calls and a stale tag can never equal the current one.  The
