@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-chunks", type=int, default=2)
+    ap.add_argument("--prefill-workload", default="qwen_prefill")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill workload (its own pool; for profiling captures)")
     return ap.parse_args()
 
 
@@ -367,7 +370,7 @@ def native_prefill(args, pool, b_p, hbm_gbs, world):
     import expert_cache_gb300 as ft
     import synth
     from expert_cache_gb300.workloads import SHAPES
-    s = SHAPES["qwen_prefill"]
+    s = SHAPES[args.prefill_workload]
     T, L = s.T, s.L
     rec = ft.ft_record_bytes(s.H, s.I)
     cache = ft.ExpertCache(L, s.E, s.H, s.I, s.k, 1, s.C, pool.ptr, T_max=T)
@@ -474,6 +477,25 @@ def native_e2e(args, s, wl, cache, graph, stream, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def prefill_only(args, world):
+    """The prefill workload alone, on a pool of its own shape."""
+    import torch
+    import expert_cache_gb300 as ft
+    from expert_cache_gb300.workloads import SHAPES, build_pool
+    s = SHAPES[args.prefill_workload]
+    pool = build_pool(args.seed, s.L, s.E, s.H, s.I)
+    probe_n = min(1 << 30, pool.nbytes)
+    probe_dev = torch.empty(probe_n, dtype=torch.uint8, device="cuda")
+    b_p = ft.ft_measure_h2d(pool.ptr, probe_dev, probe_n, 5)
+    del probe_dev
+    hbm_gbs, _, _ = peaks()
+    pf = native_prefill(args, pool, b_p, hbm_gbs, world)
+    pool.free()
+    return {"metric": "prefill tok/s (prefill-only run)", "value": pf["tok_s"], "unit": "tok/s",
+            "n_gpus": world, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": s.name}, "prefill": pf}
+
+
 # ----------------------------------------------------------------- reference arm
 
 def reference(args, rank, world):
@@ -515,7 +537,7 @@ def main():
         print(json.dumps(reference(args, rank, world)), flush=True)
         return
     rank, world = dist_setup(args)
-    out = native_decode(args, rank, world)
+    out = prefill_only(args, world) if args.prefill_only else native_decode(args, rank, world)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

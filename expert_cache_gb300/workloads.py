@@ -43,6 +43,9 @@ SHAPES = {
     "dsv4_decode": Shape("dsv4_decode", L=16, E=256, k=6, H=4096, I=2048, C=1024, B=1,
                          steps=256, p=0.8),
     "qwen_prefill": Shape("qwen_prefill", L=40, E=256, k=8, H=2048, I=512, C=600, T=8192),
+    # the same prefill layer (8192 tokens over 256 experts) for two layers only:
+    # profiling captures of the prefill kernels that hold about 2 GB on the device
+    "qwen_prefill_small": Shape("qwen_prefill_small", L=2, E=256, k=8, H=2048, I=512, C=512, T=8192),
     # the Qwen-shaped layer over a small pool (4 x 64 experts, 64 slots): profiling
     # captures of the decode kernel that hold a few hundred MB on the device
     "qwen_decode_small": Shape("qwen_decode_small", L=4, E=64, k=8, H=2048, I=512, C=64, B=1,
