@@ -76,6 +76,7 @@ _f = {
                               c_void_p, c_void_p),
     "ft_cache_capacity": _sig("ft_cache_capacity", c_int32, c_void_p, _P(c_int32)),
     "ft_cache_status": _sig("ft_cache_status", c_int32, c_void_p, _P(c_int32)),
+    "ft_check_bounded_waits": _sig("ft_check_bounded_waits", c_int32, _P(c_uint32)),
     "ft_quantize_experts": _sig("ft_quantize_experts", c_int32, c_void_p, c_void_p, c_int32,
                                 c_int32, c_int32, c_void_p, c_void_p),
     "ft_pinned_alloc": _sig("ft_pinned_alloc", c_int32, c_size_t, _P(c_void_p)),
@@ -205,6 +206,12 @@ def ft_cache_status(handle):
     s = c_int32()
     _check(_f["ft_cache_status"](handle, ctypes.byref(s)), handle)
     return s.value
+
+
+def ft_check_bounded_waits():
+    bits = c_uint32()
+    _check(_f["ft_check_bounded_waits"](ctypes.byref(bits)))
+    return bits.value
 
 
 def ft_quantize_experts(w_gu, w_d, n, H, I, records, stream=None):

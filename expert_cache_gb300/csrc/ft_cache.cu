@@ -460,6 +460,14 @@ ft_status ft_pinned_free(void* p) {
     return cudaFreeHost(p) == cudaSuccess ? FT_OK : FT_ERR_CUDA;
 }
 
+ft_status ft_check_bounded_waits(uint32_t* expired) {
+    if (!expired) return FT_ERR_ARG;
+    unsigned bits = 0;
+    if (check_bounded_waits(&bits) != cudaSuccess) return FT_ERR_CUDA;
+    *expired = bits;
+    return FT_OK;
+}
+
 ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t reps, double* gbps) {
     if (!pinned || !dev || !bytes || reps < 1 || !gbps) return FT_ERR_ARG;
     cudaStream_t s;

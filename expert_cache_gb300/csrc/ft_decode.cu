@@ -1392,4 +1392,42 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
                       decode_smem(a.H, a.I, a.E, a.R_cap), s, a);
 }
 
+// ------------------------------------------------------------------ bounded waits check
+
+// One thread runs each bounded wait of the decode kernel against a condition that
+// nothing will satisfy: a counter nobody raises (wait_geq), a word whose tag nobody
+// writes (wait_tag_acquire, fetch_tagged) and an mbarrier nobody arrives on
+// (mbar_wait).  Bit i of *expired is set when wait i gave up.
+__global__ void wait_check_kernel(const unsigned* counter, const unsigned long long* words,
+                                  unsigned* expired) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    unsigned bits = 0;
+    if (!wait_geq(counter, 1u)) bits |= 1u;
+    if (!wait_tag_acquire(words, 7u)) bits |= 2u;
+    int timeout = 0;
+    float v[8];
+    fetch_tagged<8>([&](int i) { return words + i; }, 7u, v, &timeout);
+    if (timeout) bits |= 4u;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait(&bar, 0)) bits |= 8u;
+    *expired = bits;
+}
+
+cudaError_t check_bounded_waits(unsigned* expired) {
+    // scratch: [0] counter (0), [1] result, bytes 32..95 eight words with tag 0
+    unsigned* d = nullptr;
+    cudaError_t e = cudaMalloc(&d, 256);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(d, 0, 256);
+    if (e == cudaSuccess) {
+        wait_check_kernel<<<1, 32>>>(d, reinterpret_cast<const unsigned long long*>(d + 8), d + 1);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpy(expired, d + 1, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    return e;
+}
+
 }  // namespace ft

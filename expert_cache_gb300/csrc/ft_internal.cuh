@@ -132,6 +132,7 @@ cudaError_t launch_init_tables(int32_t* slot_for_id, int n_ids, int32_t* id_of_s
 // Grid of the decode kernel for a cache shape (every CTA resident at once), and the
 // launch; both take the cache's B_max * k_max as R_cap.
 int decode_grid(int H, int I, int E, int R_cap);
+cudaError_t check_bounded_waits(unsigned* expired);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s);

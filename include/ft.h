@@ -202,6 +202,16 @@ ft_status ft_cache_capacity(const ft_cache* c, int32_t* capacity);
 /* Read and clear the device status word (FT_DEV_* bits).  Synchronises. */
 ft_status ft_cache_status(ft_cache* c, int32_t* device_status);
 
+/* Diagnostic of the failure path (no counterpart on the pages): one GPU thread runs
+ * each kind of bounded wait the decode kernel uses against a condition nothing will
+ * satisfy (a counter nobody raises, a tagged word nobody writes, read once with an
+ * acquire and once in a batch, an mbarrier nobody arrives on).  Every wait must give
+ * up after its one-second bound instead of hanging; *expired gets bit i set when wait
+ * i did, so a healthy build returns 0xF.  The kernel exits normally and the context
+ * stays usable.  Takes about 4 s; synchronises the device; needs no cache.
+ * Errors: FT_ERR_ARG for a NULL expired, FT_ERR_CUDA when the launch fails. */
+ft_status ft_check_bounded_waits(uint32_t* expired);
+
 /* Quantise n experts to NVFP4 records on the device ([EXPLAINER §8.4] layout; the
  * quantiser of the record format above, fp32 IEEE steps):
  *   s_t = amax(W)/2688; block scale = E4M3_RNE((amax16/6)/s_t);
