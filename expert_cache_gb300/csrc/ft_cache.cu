@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <new>
 
 #include "ft_internal.cuh"
@@ -49,15 +50,23 @@ WsLayout ws_layout(const ft_cache_desc& d) {
     return w;
 }
 
+// SM count of the current device (looked up once per device).
 int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
+    static std::atomic<int> n[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 1;
     }
-    return n;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (!v) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            v = 1;
+        }
+        n[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 }  // namespace ft

@@ -64,6 +64,8 @@
 // products are exact and accumulate in fp32 (fma.rn.f32.f16); each 16-element block
 // partial is scaled by its E4M3 scale in fp32; the fp32 tensor scale and the
 // prescale are applied at the end.  h stays fp32; the down GEMV is fp32 FMA.
+#include <mutex>
+
 #include "ft_internal.cuh"
 
 namespace ft {
@@ -1366,16 +1368,26 @@ static size_t decode_smem(int H, int I, int E, int R_cap) {
 }
 
 int decode_grid(int H, int I, int E, int R_cap) {
-    // the attribute is per kernel: keep it at the largest size any cache needs
-    static size_t attr_bytes = 0;
+    // the attribute is per kernel and device: keep it at the largest size any cache on
+    // the device needs
+    static std::mutex mu;
+    static size_t attr_bytes[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
     const size_t sm = decode_smem(H, I, E, R_cap);
-    if (sm > attr_bytes) {
-        if (cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sm) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (sm > attr_bytes[dev]) {
+            if (cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sm) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
+            attr_bytes[dev] = sm;
         }
-        attr_bytes = sm;
     }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kThreads, sm) !=

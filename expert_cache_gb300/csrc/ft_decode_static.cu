@@ -29,7 +29,6 @@
 namespace ft {
 
 constexpr size_t kStaticScratchBytes = (size_t)8 << 20;   // 8 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 

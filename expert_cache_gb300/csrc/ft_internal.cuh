@@ -14,6 +14,7 @@
 namespace ft {
 
 // ----------------------------------------------------------------- limits
+constexpr int kMaxDevices = 64;           // per-device host-side caches (attributes, SM count)
 constexpr int kThreadsRemap = 1024;
 constexpr int kMaxE = 4096;            // experts per layer
 constexpr int kMaxC = 16384;           // slots

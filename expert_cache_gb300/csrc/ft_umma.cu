@@ -19,7 +19,9 @@
 // accumulator (tcgen05.ld) and run the epilogue.  Every mbarrier wait is bounded:
 // on expiry the CTA records FT_DEV_TIMEOUT, drains its own copies and frees TMEM.
 #include <cuda.h>
+#include <atomic>
 #include <cstdio>
+#include <mutex>
 
 #include "ft_prefill.cuh"
 #include "ft_quant.cuh"
@@ -387,12 +389,21 @@ size_t umma_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
 
 cudaError_t launch_umma(const CUtensorMap& a, const CUtensorMap& b, const UmmaArgs& g, int grid,
                         cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)umma_smem_bytes());
-        if (e != cudaSuccess) return e;
-        attr = true;
+    // the shared-memory attribute is per device; set it once on each
+    static std::atomic<bool> attr[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr[dev].load(std::memory_order_relaxed)) {
+            e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)umma_smem_bytes());
+            if (e != cudaSuccess) return e;
+            attr[dev].store(true, std::memory_order_release);
+        }
     }
     umma_gemm_kernel<<<grid, kThreads, umma_smem_bytes(), s>>>(a, b, g);
     return cudaGetLastError();
