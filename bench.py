@@ -476,7 +476,10 @@ def native_e2e(args, s, wl, cache, graph, stream, world):
     h2d = dx.numel() * dx.element_size() + di.numel() * 4 + dw.numel() * 4
     d2h = dy.numel() * 4
     return {"value": args.steps * s.B * world / (ms / 1e3), "unit": "tok/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "the same steps timed in a separate pass after the device-timed one; the "
+                    "fills' host-link rate varies between passes on a shared host, by more "
+                    "than the step's few hundred KB of copies cost"}
 
 
 def prefill_only(args, world):
