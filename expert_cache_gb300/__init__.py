@@ -234,8 +234,13 @@ def ft_measure_h2d(pinned, dev, nbytes, reps=5):
     return g.value
 
 
-def ft_profile_enable(handle, enable=True):
-    _check(_f["ft_profile_enable"](handle, 1 if enable else 0), handle)
+FT_PROF_ALL = (1 << FT_PROF_KINDS) - 1
+
+
+def ft_profile_enable(handle, kinds=True):
+    """kinds: True (all kinds), False (off) or a bit mask of kinds (bit i: kind i)."""
+    mask = FT_PROF_ALL if kinds is True else (0 if kinds is False else int(kinds))
+    _check(_f["ft_profile_enable"](handle, mask), handle)
 
 
 def ft_profile_read(handle):

@@ -211,7 +211,7 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
     c->workspace = static_cast<uint8_t*>(d->workspace);
     c->buffer_layer[0] = c->buffer_layer[1] = -1;
     c->copy_pending = false;
-    c->prof = false;
+    c->prof = 0;
     c->prof_n = 0;
     c->err[0] = 0;
     c->grid_decode = decode_grid(d->H, d->I, d->E, d->B_max * d->k_max);
@@ -300,9 +300,9 @@ uint32_t ft_split_from_overlap(double p_ov, double c_ov) {
 
 static void prof_fold(ft_cache* c) {
     if (c->prof_n == 0) return;
-    cudaEventSynchronize(c->prof_ev[2 * c->prof_n - 1]);
     for (int i = 0; i < c->prof_n; ++i) {
         float ms = 0.f;
+        cudaEventSynchronize(c->prof_ev[2 * i + 1]);   // pairs may sit on different streams
         if (cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]) == cudaSuccess) {
             c->prof_ms[c->prof_kind[i]] += ms;
             c->prof_launches[c->prof_kind[i]] += 1;
@@ -313,7 +313,7 @@ static void prof_fold(ft_cache* c) {
 
 // Records the "before" event of a launch of `kind`; returns the pair index or -1.
 static int prof_begin(ft_cache* c, int kind, cudaStream_t s) {
-    if (!c->prof) return -1;
+    if (!(c->prof & (1u << kind))) return -1;
     if (c->prof_n * 2 + 2 > ft_cache::kProfEvents) prof_fold(c);
     const int i = c->prof_n++;
     c->prof_kind[i] = kind;
@@ -332,7 +332,7 @@ ft_status ft_profile_enable(ft_cache* c, int32_t enable) {
             if (cudaEventCreate(&c->prof_ev[i]) != cudaSuccess) return FT_ERR_CUDA;
     }
     if (!enable) prof_fold(c);
-    c->prof = enable != 0;
+    c->prof = (unsigned)enable & ((1u << FT_PROF_KINDS) - 1);
     return FT_OK;
 }
 

@@ -221,7 +221,7 @@ struct ft_cache {
     bool maps_ok;
     int grid_decode;
     // profiling
-    bool prof;
+    unsigned prof;          // bit i set: time launches of kind i
     static constexpr int kProfEvents = 65536;
     cudaEvent_t prof_ev[kProfEvents];
     int prof_kind[kProfEvents / 2];

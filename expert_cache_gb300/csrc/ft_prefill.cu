@@ -50,7 +50,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     auto copy_layer = [&](int l, int buf) -> cudaError_t {
         cudaStreamWaitEvent(c->copy_stream, c->entry_ev, 0);
         cudaEvent_t e1 = nullptr;
-        if (c->prof && c->prof_n * 2 + 2 <= ft_cache::kProfEvents) {
+        if ((c->prof & (1u << 4)) && c->prof_n * 2 + 2 <= ft_cache::kProfEvents) {
             const int i = c->prof_n++;
             c->prof_kind[i] = 4;
             cudaEventRecord(c->prof_ev[2 * i], c->copy_stream);
@@ -117,7 +117,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
 
     auto prof_kernel = [&](int kind, auto&& launch) -> cudaError_t {
         cudaEvent_t e0 = nullptr, e1 = nullptr;
-        if (c->prof) {
+        if (c->prof & (1u << kind)) {
             if (c->prof_n * 2 + 2 > ft_cache::kProfEvents) return cudaErrorInvalidValue;
             const int i = c->prof_n++;
             c->prof_kind[i] = kind;

@@ -234,9 +234,12 @@ ft_status ft_measure_h2d(const void* pinned, void* dev, size_t bytes, int32_t re
 /* Per-kernel device time accumulated while profiling is on (CUDA events around
  * each launch on the launching stream).  kind: 0 decode layer kernel, 1 prefill
  * GEMM1, 2 prefill GEMM2, 3 prefill other kernels, 4 prefill layer copies (on the
- * cache's copy stream). */
+ * cache's copy stream).  kinds: bit mask, bit i times launches of kind i (0: off,
+ * FT_PROF_ALL: every kind).  Timing only the copies (kinds = 1 << 4) records events
+ * on the copy stream alone and leaves the compute stream's launches untouched. */
 #define FT_PROF_KINDS 5
-ft_status ft_profile_enable(ft_cache* c, int32_t enable);
+#define FT_PROF_ALL ((1 << FT_PROF_KINDS) - 1)
+ft_status ft_profile_enable(ft_cache* c, int32_t kinds);
 ft_status ft_profile_read(ft_cache* c, double* total_ms /*[FT_PROF_KINDS]*/,
                           int64_t* launches /*[FT_PROF_KINDS]*/);
 

@@ -98,7 +98,8 @@ def decode_layer_dense(x, ids, gates, layer, E, experts: RecordSource, shared=No
 
 # ---------------------------------------------------------------- prefill
 
-def prefill_layer(x, ids, gates, layer: int, E: int, experts: RecordSource):
+def prefill_layer(x, ids, gates, layer: int, E: int, experts: RecordSource,
+                  return_h32: bool = False):
     """Prefill expert compute for one layer with NVFP4 activations on both GEMMs.
 
     x [T, H] (bf16 values) is quantised with the unit-tensor-scale activation
@@ -107,7 +108,9 @@ def prefill_layer(x, ids, gates, layer: int, E: int, experts: RecordSource):
     o = W_d h_q; y[t] = sum_j gates[t,j] * o_(t,j) in route order j = 0..k-1.
 
     Returns (y [T, H] fp64, h_codes [T*k, I] uint8, h_scales [T*k, I/16] uint8),
-    h indexed by route r = t*k + j (rows of masked routes are zero).
+    h indexed by route r = t*k + j (rows of masked routes are zero); with
+    return_h32 also the fp32 h [T*k, I] that was quantised (the value whose
+    distance to a rounding boundary decides a code).
     """
     x = np.asarray(x, np.float32)
     ids = np.asarray(ids, np.int64)
@@ -117,6 +120,7 @@ def prefill_layer(x, ids, gates, layer: int, E: int, experts: RecordSource):
     I = experts.I
     h_codes = np.zeros((T * k, I), np.uint8)
     h_scales = np.zeros((T * k, I // 16), np.uint8)
+    h32_all = np.zeros((T * k, I), np.float32) if return_h32 else None
     for e in range(E):
         t_idx, j_idx = np.nonzero(ids == e)
         if t_idx.size == 0:
@@ -129,7 +133,11 @@ def prefill_layer(x, ids, gates, layer: int, E: int, experts: RecordSource):
         r = t_idx * k + j_idx
         h_codes[r] = hc
         h_scales[r] = hs
+        if return_h32:
+            h32_all[r] = h32
     y = prefill_from_h(h_codes, h_scales, ids, gates, layer, E, experts)
+    if return_h32:
+        return y, h_codes, h_scales, h32_all
     return y, h_codes, h_scales
 
 

@@ -130,3 +130,134 @@ def test_prefill_routes_are_topk_of_logits():
     assert all(len(set(r)) == 4 for r in ids.tolist())
     assert np.allclose(gates.numpy().sum(1), 1.0, atol=1e-6)
     assert np.all(np.diff(gates.numpy(), axis=1) <= 0)      # sorted by logit
+
+
+# ---------------------------------------------------------------- prefill closed form
+#
+# Every value below is chosen so that both activation quantisations are exact or
+# decided by a known rounding rule, and y is exact in fp64:
+#   * token t has one non-zero x element, 6.0 at column c_t of the first 16-block:
+#     amax 6 -> scale E4M3(1.0) (code 0x38), code of 6.0; the other blocks have
+#     amax 0 -> scale 0, a zero block.  So g_i = 6 * Wg[i, c_t], u_i = 6 * Wu[i, c_t].
+#   * "on" rows: Wg = 4 -> g = 24, silu(24) = 24 (1 - 3.8e-11), so the fp32 h is
+#     exactly 144 * Wu (the relative deviation is far below half an fp32 ulp).
+#     Each 16-row block of h holds one row with |Wu| = 6, so amax = 864, the block
+#     scale is E4M3(864 / 6) = E4M3(144) = 144 exactly (code 0x71) and the code of an
+#     on row is the code of Wu itself.
+#   * the "mid" row: Wg = 3, Wu = 1 -> h = silu(18) * 6 = 108 (1 - 1.5e-8) in fp64,
+#     which rounds to exactly 108.0 in fp32; 108 / 144 = 0.75 is the tie between
+#     E2M1 0.5 and 1.0 and goes to the even code 2 (1.0).  Quantising the unrounded
+#     fp64 value instead would give 0.5 (code 1).
+#   * "neg" rows: Wg = -4 -> g = -24, |h| < 1e-8 -> code 0 (zero magnitudes are +0).
+#   * "zero" rows: Wg = 0 -> h = 0 -> code 0.
+# Gates are dyadic and not 1: a gate applied before h is quantised changes the
+# block scale (0.75 * 864 / 6 = 108 is not an E4M3 value), so h codes catch it.
+
+_E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _fp4_code(v):
+    c = _E2M1_VALUES.index(abs(v))
+    return c | (8 if v < 0 and c else 0)
+
+
+def _fp4_value(c):
+    return (-1.0 if c & 8 else 1.0) * _E2M1_VALUES[c & 7]
+
+
+def _prefill_fixture():
+    Hh, Ii, Ee, T, k = 64, 32, 4, 3, 2
+    cols = [1, 6, 11]                                  # c_t, all in x's first 16-block
+    ids = np.array([[0, 1], [1, 2], [3, 0]])
+    gates = np.float32([[0.75, 0.25], [0.625, 0.375], [0.8125, 0.1875]])
+    rng = np.random.default_rng(7)
+    ladder = [0.5, -1.0, 1.5, -2.0, 3.0, -4.0, 0.5, 2.0, -1.5, 1.0]
+    recs, h_want = [], {}
+    for e in range(Ee):
+        gu = rng.integers(0, 16, (2 * Ii, Hh)).astype(np.uint8)   # columns x never uses
+        d = rng.integers(0, 16, (Hh, Ii)).astype(np.uint8)
+        for c in cols:
+            want = []
+            for i in range(Ii):
+                b, r = divmod(i, 16)
+                if r == 0:                                   # on, |Wu| = 6: sets amax
+                    wg, wu, code = 4.0, (6.0 if (e + c + b) % 2 else -6.0), None
+                elif r <= 10:                                # on, varied Wu
+                    wg, wu, code = 4.0, ladder[(r - 1 + e + c) % 10], None
+                elif r == 11:                                # mid: the fp32 tie
+                    wg, wu, code = 3.0, 1.0, 2
+                elif r == 12:                                # neg, u > 0
+                    wg, wu, code = -4.0, 2.0, 0
+                elif r == 13:                                # neg, u < 0
+                    wg, wu, code = -4.0, -3.0, 0
+                elif r == 14:                                # zero gate
+                    wg, wu, code = 0.0, 1.5, 0
+                else:                                        # on, small
+                    wg, wu, code = 4.0, -0.5, None
+                gu[i, c] = _fp4_code(wg)
+                gu[Ii + i, c] = _fp4_code(wu)
+                want.append(_fp4_code(wu) if code is None else code)
+            h_want[(e, c)] = want
+        recs.append(_record_from_codes(gu, d))
+    x = np.zeros((T, Hh), np.float32)
+    for t, c in enumerate(cols):
+        x[t, c] = 6.0
+    return Hh, Ii, Ee, T, k, cols, ids, gates, recs, h_want
+
+
+def test_prefill_closed_form():
+    Hh, Ii, Ee, T, k, cols, ids, gates, recs, h_want = _prefill_fixture()
+    x = np.zeros((T, Hh), np.float32)
+    for t, c in enumerate(cols):
+        x[t, c] = 6.0
+    src = RecordSource(lambda f: recs[f], Hh, Ii)
+    y, hc, hs, h32 = prefill_layer(x, ids, gates, 0, Ee, src, return_h32=True)
+    # h per route row r = t*k + j: the codes worked out above, scale 144 (0x71)
+    for t in range(T):
+        for j in range(k):
+            r = t * k + j
+            want = h_want[(int(ids[t, j]), cols[t])]
+            assert hc[r].tolist() == want, f"h codes of route ({t}, {j})"
+            assert hs[r].tolist() == [0x71, 0x71], f"h scales of route ({t}, {j})"
+            assert h32[r][11] == np.float32(108.0) and h32[r][27] == np.float32(108.0)
+    # y by hand: o = W_d . hq with hq = code value * 144, then the gated sum over j
+    d_vals = [F.unpack_nibbles(rec[F.record_layout(Hh, Ii)["d_codes"][0]:][:Hh * Ii // 2]
+                               .reshape(Hh, Ii // 2)) for rec in recs]
+    for t in range(T):
+        want_y = [0.0] * Hh
+        for j in range(k):
+            e = int(ids[t, j])
+            hq = [_fp4_value(cd) * 144.0 for cd in h_want[(e, cols[t])]]
+            for row in range(Hh):
+                o = sum(_fp4_value(int(d_vals[e][row, i])) * hq[i] for i in range(Ii))
+                want_y[row] += float(gates[t, j]) * o
+        assert y[t].tolist() == want_y, f"y of token {t}"
+    # the second GEMM alone, from the same h
+    assert np.array_equal(prefill_from_h(hc, hs, ids, gates, 0, Ee, src), y)
+
+
+def test_prefill_closed_form_masks_and_order():
+    """A route whose id is outside [0, E) contributes nothing and leaves its h row
+    zero; swapping the two routes of a token (ids and gates together) moves the h
+    rows to the swapped route indices and leaves y unchanged."""
+    Hh, Ii, Ee, T, k, cols, ids, gates, recs, h_want = _prefill_fixture()
+    x = np.zeros((T, Hh), np.float32)
+    for t, c in enumerate(cols):
+        x[t, c] = 6.0
+    src = RecordSource(lambda f: recs[f], Hh, Ii)
+    y, hc, hs = prefill_layer(x, ids, gates, 0, Ee, src)
+    ids_sw, gates_sw = ids[:, ::-1].copy(), gates[:, ::-1].copy()
+    y2, hc2, hs2 = prefill_layer(x, ids_sw, gates_sw, 0, Ee, src)
+    for t in range(T):
+        assert np.array_equal(hc2[t * k], hc[t * k + 1]) and np.array_equal(hc2[t * k + 1], hc[t * k])
+    assert np.allclose(y2, y, rtol=1e-15, atol=0)
+    ids_m = ids.copy()
+    ids_m[1, 0] = Ee                                       # masked route (1, 0)
+    y3, hc3, hs3 = prefill_layer(x, ids_m, gates, 0, Ee, src)
+    assert not hc3[1 * k + 0].any() and not hs3[1 * k + 0].any()
+    assert np.array_equal(y3[[0, 2]], y[[0, 2]])
+    # token 1 keeps only route (1, 1): y = gate * o of that route (a one-route
+    # layer over that route's h row)
+    only = prefill_from_h(hc[[1 * k + 1]], hs[[1 * k + 1]], np.array([[ids[1, 1]]]),
+                          gates[1:2, 1:2], 0, Ee, src)
+    assert np.array_equal(y3[1], only[0])
