@@ -20,6 +20,7 @@ FT_OK, FT_ERR_ARG, FT_ERR_CUDA, FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, F
 FT_DEV_BAD_ID, FT_DEV_TIMEOUT = 0x1, 0x2
 FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR = 0, 1
 FT_PREFILL_DOUBLE_BUFFER = 1
+FT_PREFILL_DEBUG_X = 2
 FT_PROF_KINDS = 5
 PROF_NAMES = ("decode", "prefill_gemm1", "prefill_gemm2", "prefill_other", "prefill_copy")
 
@@ -74,6 +75,9 @@ _f = {
                                  c_void_p, c_void_p),
     "ft_cache_snapshot": _sig("ft_cache_snapshot", c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p),
+    "ft_cache_restore": _sig("ft_cache_restore", c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_int64, c_void_p),
+    "ft_cache_set_trace": _sig("ft_cache_set_trace", c_int32, c_void_p, c_void_p, c_int32),
     "ft_cache_capacity": _sig("ft_cache_capacity", c_int32, c_void_p, _P(c_int32)),
     "ft_cache_status": _sig("ft_cache_status", c_int32, c_void_p, _P(c_int32)),
     "ft_check_bounded_waits": _sig("ft_check_bounded_waits", c_int32, _P(c_uint32)),
@@ -200,6 +204,36 @@ def ft_cache_snapshot(handle, L, E):
     _check(_f["ft_cache_snapshot"](handle, sfi.ctypes.data, ios.ctypes.data, usage.ctypes.data,
                                    tick.ctypes.data), handle)
     return sfi, ios, usage, int(tick[0])
+
+
+def ft_cache_restore(handle, slot_for_id, id_of_slot, usage, tick, stream=None):
+    sfi = np.ascontiguousarray(slot_for_id, np.int32)
+    ios = np.ascontiguousarray(id_of_slot, np.int32)
+    us = np.ascontiguousarray(usage, np.int64)
+    _check(_f["ft_cache_restore"](handle, sfi.ctypes.data, ios.ctypes.data, us.ctypes.data,
+                                  int(tick), _stream(stream)), handle)
+
+
+# one stats-ring record: tick, layer, n_hit, m, q, n_def_routes, n_units, t_commit_ns
+TRACE_DTYPE = np.dtype([("tick", np.int64), ("layer", np.int32), ("n_hit", np.int32),
+                        ("m", np.int32), ("q", np.int32), ("n_def_routes", np.int32),
+                        ("n_units", np.int32), ("t_commit_ns", np.int64)])
+TRACE_HEADER_BYTES = 16
+
+
+def ft_cache_set_trace(handle, ring, capacity):
+    _check(_f["ft_cache_set_trace"](handle, _ptr(ring), int(capacity)), handle)
+
+
+def trace_records(ring_bytes: np.ndarray, capacity: int):
+    """(count, records in write order) of a stats ring copied to the host."""
+    count = int(ring_bytes[:8].view(np.uint64)[0])
+    recs = ring_bytes[TRACE_HEADER_BYTES:TRACE_HEADER_BYTES + capacity * TRACE_DTYPE.itemsize]
+    recs = recs.view(TRACE_DTYPE)
+    n = min(count, capacity)
+    start = count % capacity if count > capacity else 0
+    order = [(start + i) % capacity for i in range(n)]
+    return count, recs[order]
 
 
 def ft_cache_status(handle):

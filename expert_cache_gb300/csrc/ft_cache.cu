@@ -137,6 +137,8 @@ DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids
     a.deferred = deferred;
     a.route_slot = route_slot;
     a.counters = counters;
+    a.trace = static_cast<unsigned long long*>(c->trace);
+    a.trace_cap = c->trace ? (unsigned)c->trace_cap : 0u;
     return a;
 }
 
@@ -213,6 +215,8 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
     c->copy_pending = false;
     c->prof = 0;
     c->prof_n = 0;
+    c->trace = nullptr;
+    c->trace_cap = 0;
     c->err[0] = 0;
     c->grid_decode = decode_grid(d->H, d->I, d->E, d->B_max * d->k_max);
     if (c->grid_decode < 2) {
@@ -311,8 +315,12 @@ static void prof_fold(ft_cache* c) {
     c->prof_n = 0;
 }
 
+}  // extern "C"
+
+namespace ft {
+
 // Records the "before" event of a launch of `kind`; returns the pair index or -1.
-static int prof_begin(ft_cache* c, int kind, cudaStream_t s) {
+int prof_begin(ft_cache* c, int kind, cudaStream_t s) {
     if (!(c->prof & (1u << kind))) return -1;
     if (c->prof_n * 2 + 2 > ft_cache::kProfEvents) prof_fold(c);
     const int i = c->prof_n++;
@@ -321,9 +329,13 @@ static int prof_begin(ft_cache* c, int kind, cudaStream_t s) {
     return i;
 }
 
-static void prof_end(ft_cache* c, int i, cudaStream_t s) {
+void prof_end(ft_cache* c, int i, cudaStream_t s) {
     if (i >= 0) cudaEventRecord(c->prof_ev[2 * i + 1], s);
 }
+
+}  // namespace ft
+
+extern "C" {
 
 ft_status ft_profile_enable(ft_cache* c, int32_t enable) {
     if (!c) return FT_ERR_ARG;
@@ -427,6 +439,59 @@ ft_status ft_cache_snapshot(ft_cache* c, int32_t* slot_for_id, int32_t* id_of_sl
     if (e == cudaSuccess && tick)
         e = cudaMemcpy(tick, ws + c->ws.scalars + offsetof(DevScalars, tick), 8, cudaMemcpyDeviceToHost);
     return e == cudaSuccess ? FT_OK : cuda_fail(c, e, "snapshot");
+}
+
+ft_status ft_cache_restore(ft_cache* c, const int32_t* slot_for_id, const int32_t* id_of_slot,
+                           const int64_t* usage, int64_t tick, void* stream) {
+    if (!c) return FT_ERR_ARG;
+    if (!slot_for_id || !id_of_slot || !usage || tick < 0) return fail(c, FT_ERR_ARG, "NULL table or tick < 0");
+    const int C = c->C;
+    const long long n_ids = (long long)c->d.L * c->d.E;
+    // consistency of the tables (host side, before anything is written)
+    for (int s = 0; s < C; ++s) {
+        const int f = id_of_slot[s];
+        if (f < -1 || f >= n_ids) return fail(c, FT_ERR_ARG, "id_of_slot entry out of range");
+        if (f >= 0 && slot_for_id[f] != s) return fail(c, FT_ERR_ARG, "id_of_slot / slot_for_id disagree");
+        if (f < 0 && usage[s] != -1) return fail(c, FT_ERR_ARG, "free slot with usage != -1");
+        if (f >= 0 && (usage[s] < 0 || usage[s] > tick)) return fail(c, FT_ERR_ARG, "usage outside [0, tick]");
+    }
+    for (long long f = 0; f < n_ids; ++f) {
+        const int s = slot_for_id[f];
+        if (s < -1 || s >= C) return fail(c, FT_ERR_ARG, "slot_for_id entry out of range");
+        if (s >= 0 && id_of_slot[s] != f) return fail(c, FT_ERR_ARG, "slot_for_id / id_of_slot disagree");
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cuda_fail(c, cudaGetLastError(), "capture query");
+    if (cs != cudaStreamCaptureStatusNone) return fail(c, FT_ERR_STATE, "restore while capturing");
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->copy_stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "restore drain");
+    // LRU order: free slots ascending, then ascending (usage, slot)
+    int32_t* order = new (std::nothrow) int32_t[C];
+    if (!order) return fail(c, FT_ERR_ARG, "host allocation for the LRU order failed");
+    for (int s = 0; s < C; ++s) order[s] = s;
+    std::stable_sort(order, order + C, [&](int a, int b) { return usage[a] < usage[b]; });
+    uint8_t* ws = c->workspace;
+    e = cudaMemcpy(ws + c->ws.slot_for_id, slot_for_id, (size_t)n_ids * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(ws + c->ws.id_of_slot, id_of_slot, (size_t)C * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(ws + c->ws.usage, usage, (size_t)C * 8, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(ws + c->ws.lru_order, order, (size_t)C * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ws + c->ws.scalars + offsetof(DevScalars, tick), &tick, 8, cudaMemcpyHostToDevice);
+    delete[] order;
+    if (e != cudaSuccess) return cuda_fail(c, e, "restore copy");
+    c->buffer_layer[0] = c->buffer_layer[1] = -1;
+    c->copy_pending = false;
+    return FT_OK;
+}
+
+ft_status ft_cache_set_trace(ft_cache* c, void* ring, int32_t capacity) {
+    if (!c || capacity < 0) return FT_ERR_ARG;
+    if (ring && !aligned(ring, 16)) return fail(c, FT_ERR_ARG, "trace ring must be 16-byte aligned");
+    c->trace = capacity > 0 ? ring : nullptr;
+    c->trace_cap = c->trace ? capacity : 0;
+    return FT_OK;
 }
 
 ft_status ft_cache_status(ft_cache* c, int32_t* device_status) {

@@ -1230,6 +1230,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
                 a.counters[3] = nd;
             }
             if (S.bad) atomicOr(&a.sc->status, FT_DEV_BAD_ID);
+            if (a.trace) {   // per-call stats ring: 16-byte header, then the records
+                const unsigned long long i = atomicAdd(a.trace, 1ull);
+                ft_trace_rec* rec = reinterpret_cast<ft_trace_rec*>(a.trace + 2) + (i % a.trace_cap);
+                rec->tick = S.tick;
+                rec->layer = a.layer;
+                rec->n_hit = n_hit;
+                rec->m = S.m;
+                rec->q = q;
+                rec->n_def_routes = nd;
+                rec->n_units = n_units;
+                rec->t_commit_ns = (long long)gtime();
+            }
         }
         for (int i = tid; i < q; i += kThreads) v_old[i] = a.id_of_slot[D.u_s[i]];
         // touched slots: the hits' and the victims'
@@ -1398,10 +1410,25 @@ int decode_grid(int H, int I, int E, int R_cap) {
     return sm_count() * per_sm;
 }
 
+// The CTAs of one launch wait on each other's flags, so all of them must be resident
+// at once: the launch is cooperative (the driver starts it only when the whole grid
+// fits, and fails it otherwise) as well as a programmatic dependent of the previous
+// kernel on the stream.
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
     if (grid < 2) return cudaErrorInvalidConfiguration;
-    return launch_pdl(decode_layer_kernel, dim3(grid), dim3(kThreads),
-                      decode_smem(a.H, a.I, a.E, a.R_cap), s, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = decode_smem(a.H, a.I, a.E, a.R_cap);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
 }
 
 // ------------------------------------------------------------------ bounded waits check

@@ -75,11 +75,11 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     size_t off = 0;
     const size_t o_sync = off;   off = up256(off + kSyncWords * 4);
     const size_t o_h = off;      off = up256(off + P * (size_t)c->d.I * 8);
-    const size_t U = (size_t)c->d.B_max * c->d.k_max + 1;
+    const size_t U = (size_t)B * k + 1;                 // units of this call: <= B*k + shared
     const size_t o_hf = off;     off = up256(off + U * (size_t)(c->d.I / decode_pairs(c->d.H)) * 8);
     const size_t o_yf = off;     off = up256(off + (size_t)(c->d.H / decode_rows(c->d.I)) * 8);
     if (off > kStaticScratchBytes)
-        return fail(FT_ERR_ARG, "B, k and I need more than the 8 MiB static scratch");
+        return fail(FT_ERR_ARG, "B, k, H and I need more than the 8 MiB static scratch");
     uint8_t* scr = scratch_address();
     if (!scr) return fail(FT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
 
@@ -99,7 +99,9 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     a.yflag = reinterpret_cast<unsigned long long*>(scr + o_yf);
     a.scrub = reinterpret_cast<unsigned long long*>(scr + o_h);
     a.scrub_words = (kStaticScratchBytes - o_h) / 8;
+    const int p = prof_begin(c, 0, s);
     const cudaError_t e = launch_decode(a, c->grid_decode, s);
+    prof_end(c, p, s);
     if (e != cudaSuccess) {
         snprintf(c->err, sizeof(c->err), "static decode launch: %s", cudaGetErrorString(e));
         return FT_ERR_CUDA;

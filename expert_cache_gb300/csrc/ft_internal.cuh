@@ -124,6 +124,8 @@ struct DecodeArgs {
     int32_t* deferred;
     int32_t* route_slot;
     int32_t* counters;
+    unsigned long long* trace;  // stats ring header (count), or nullptr
+    unsigned trace_cap;         // records after the 16-byte header
 };
 
 // Kernel launchers (each returns the launch error).
@@ -220,6 +222,8 @@ struct ft_cache {
     CUtensorMap map_a2, map_b2;     // GEMM2: quantised h rows; W_d codes of the slots
     bool maps_ok;
     int grid_decode;
+    void* trace;                    // per-call stats ring (device) or nullptr
+    int trace_cap;
     // profiling
     unsigned prof;          // bit i set: time launches of kind i
     static constexpr int kProfEvents = 65536;
@@ -232,6 +236,10 @@ struct ft_cache {
 };
 
 namespace ft {
+// CUDA-event timing of a launch of `kind` on stream s while profiling that kind is
+// on: prof_begin returns the event pair index (or -1), prof_end closes it.
+int prof_begin(ft_cache* c, int kind, cudaStream_t s);
+void prof_end(ft_cache* c, int i, cudaStream_t s);
 // Arguments of a decode call on cache c except the per-call scratch (h, o, sync).
 DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids, const float* w,
                        int B, int k, float* y, int32_t* deferred, int32_t* route_slot,

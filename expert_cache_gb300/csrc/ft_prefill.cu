@@ -132,6 +132,18 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
 
     e = prof_kernel(3, [&] { return launch_pf_sort_quant(a, s); });
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "route sort launch");
+    if (debug_h && (flags & FT_PREFILL_DEBUG_X)) {
+        // the quantised activations as the GEMM reads them (sorted rows) and the
+        // sorted row of every route, after the h region of the debug buffer
+        uint8_t* dx = static_cast<uint8_t*>(debug_h) + RT * (d.I / 2 + d.I / 16);
+        e = cudaMemcpyAsync(dx, a.route_pos, RT * 4, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dx + RT * 4, a.a_codes, RT * (d.H / 2), cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dx + RT * (4 + d.H / 2), a.a_scales, RT * (d.H / 16),
+                                cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return fail(FT_ERR_CUDA, "debug copy of the quantised x");
+    }
 
     UmmaArgs g;
     g.E = d.E;

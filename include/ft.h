@@ -164,8 +164,10 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
  * address is looked up on the first call made on each device, so make that first
  * call before any stream capture.  Every call shares the array: calls that
  * overlap on the GPU race and must be serialised by the caller.  Errors: those of
- * ft_moe_decode, and FT_ERR_ARG when B, k and I need more than 8 MiB of scratch
- * (about (B*k + B) * I * 8 bytes). */
+ * ft_moe_decode, and FT_ERR_ARG when B, k, H and I need more than 8 MiB of scratch:
+ * (B*k + B) * I * 8 bytes of h words, (B*k + 1) * (I / pairs) * 8 bytes of item flags
+ * and (H / rows) * 8 bytes of tile flags, each region rounded up to 256 bytes, plus
+ * 256 bytes of grid state (pairs = 16 and rows = 64 at the benchmark shapes). */
 ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t B,
                                int32_t k, float* y, int32_t* deferred, int32_t* route_slot,
@@ -182,9 +184,15 @@ ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
  *   x         device bf16 [T, H];  topk_ids device int32 [T, k];  topk_w device fp32 [T, k]
  *   y         device fp32 [T, H], overwritten
  *   debug_h   device uint8 or NULL: per route r = t*k + j, I/2 packed h codes followed
- *             (after all T*k rows) by [T*k, I/16] h scales
+ *             (after all T*k rows) by [T*k, I/16] h scales.  With FT_PREFILL_DEBUG_X
+ *             in flags, the same buffer continues with the quantised activations as
+ *             the GEMM reads them: int32 [T*k] sorted row of each route (-1: masked
+ *             route), then [T*k, H/2] packed x codes and [T*k, H/16] x scales in
+ *             sorted-row order (rows past the last valid route are unspecified).
+ *             Total bytes: T*k*(I/2 + I/16 + 4 + H/2 + H/16).
  * Calls for one chunk go layer 0, 1, ..., L-1 on the same stream. */
 #define FT_PREFILL_DOUBLE_BUFFER 1
+#define FT_PREFILL_DEBUG_X       2
 ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t T,
                                int32_t k, float* y, int32_t flags, void* debug_h,
@@ -195,6 +203,35 @@ ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void* x,
  * resize), tick.  Any output may be NULL. */
 ft_status ft_cache_snapshot(ft_cache* c, int32_t* slot_for_id, int32_t* id_of_slot,
                             int64_t* usage, int64_t* tick);
+
+/* Load the tables from host arrays, the inverse of ft_cache_snapshot (for replaying a
+ * run from a saved point; the slot contents are not saved, so every occupied slot
+ * must already hold its expert's record, e.g. the buffer the snapshot was taken
+ * over).  Synchronous safe-point call like ft_cache_resize: synchronises `stream`
+ * and the copy stream, then writes slot_for_id [L*E], id_of_slot [C], usage [C] and
+ * the tick, and rebuilds the LRU order (free slots ascending, then ascending
+ * (usage, slot)).  The arrays must be consistent: id_of_slot[s] in [-1, L*E),
+ * slot_for_id[f] in [-1, C), slot_for_id[id_of_slot[s]] == s for every occupied s
+ * and id_of_slot[slot_for_id[f]] == f for every mapped f, usage -1 exactly on free
+ * slots and in [0, tick] elsewhere.  Errors: FT_ERR_ARG (NULL array, inconsistent
+ * tables), FT_ERR_STATE (stream is being captured), FT_ERR_CUDA. */
+ft_status ft_cache_restore(ft_cache* c, const int32_t* slot_for_id, const int32_t* id_of_slot,
+                           const int64_t* usage, int64_t tick, void* stream);
+
+/* Per-call stats ring (device).  When set, every decode call (ft_moe_decode,
+ * ft_moe_decode_static) appends one record from its commit step: the call's tick,
+ * layer, |H|, m, q, deferred routes, the number of GPU experts computed (hits +
+ * fills + the shared expert) and the GPU's %globaltimer at the commit (ns).
+ * ring: device memory of 16 + capacity * sizeof(ft_trace_rec) bytes, 16-byte
+ * aligned, zeroed by the caller: uint64 count (records ever written), 8 bytes
+ * reserved, then the records; record i lands at index i mod capacity.  ring NULL or
+ * capacity 0 switches the ring off.  Only later calls see the change. */
+typedef struct {
+    int64_t tick;
+    int32_t layer, n_hit, m, q, n_def_routes, n_units;
+    int64_t t_commit_ns;
+} ft_trace_rec;
+ft_status ft_cache_set_trace(ft_cache* c, void* ring, int32_t capacity);
 
 /* Current slot count. */
 ft_status ft_cache_capacity(const ft_cache* c, int32_t* capacity);

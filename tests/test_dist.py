@@ -60,3 +60,5 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "tok/s" and d["value"] > 0
     assert d["config"]["workload"] == "tiny" and d["steps"] == 2
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["product_libraries_loaded"] == []            # the oracle arm maps no product library
+    assert d["ms_per_step"] * d["steps"] / 1e3 <= 300

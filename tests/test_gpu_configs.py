@@ -53,8 +53,9 @@ def _check_calls(wl, ref, t0, t1, samples, experts):
                 assert_close(y + y_cpu, y_ref, f"step {t} layer {l} token {b}")
 
 
-@pytest.mark.parametrize("B,f", [(1, 2 / 3), (4, 0.5), (4, 0.25)])
-def test_dsv4_shaped_decode(ft, dsv4_pool, B, f):
+@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("f", [2 / 3, 0.5, 0.25])
+def test_dsv4_shaped_decode(ft, dsv4_pool, f, B):
     """16 layers x 256 experts (H 4096, I 2048), 1024 slots, locality 0.8, q* split
     with f = B_P / B_H for B_H / B_P in {1.5, 2, 4}, batch 1 and 4."""
     from dataclasses import replace

@@ -191,33 +191,107 @@ def test_resize_matches_oracle(ft, wl_mod):
     pool.free()
 
 
-def test_qwen_shaped_decode_full_size(ft, wl_mod):
-    """Config at full size (40 x 256 experts, H 2048, I 512, 600 slots, shared expert),
-    in the launch configuration the benchmark times: state on every call, outputs on
-    sampled (step, layer) pairs."""
+@pytest.fixture(scope="module")
+def qwen_pool(wl_mod):
     s = wl_mod.SHAPES["qwen_decode"]
-    steps = 48
     pool = wl_mod.build_pool(0, s.L, s.E, s.H, s.I)
     shared = wl_mod.build_shared(0, s.L, s.H, s.I)
-    for mode in ("full", "qstar"):
-        split = wl_mod.split_tuple(mode, 32768)
-        cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool.ptr, shared=shared, split=split)
-        wl = wl_mod.DecodeWorkload(s, seed=0, steps=steps)
-        ref = SlotCache(s.L, s.E, s.C, full_offload=(mode == "full"), f_q16=32768)
-        for t in range(steps):
-            wl.run_step(cache, t)
-        torch.cuda.synchronize()
-        experts = oracle_experts(0, s.H, s.I)
-        sample = {(0, 0), (1, 17), (5, 39), (31, 3), (steps - 1, 20)}
-        shared_cache = {}
-        for t in range(steps):
-            for l in range(s.L):
-                r = _check_call(ft, wl, ref, t, l)
-                if (t, l) in sample:
-                    if l not in shared_cache:
-                        shared_cache[l] = oracle_shared(0, l, s.H, s.I)
-                    _check_output(wl, r, t, l, experts, shared_cache[l])
-        for a, b in zip(ft.ft_cache_snapshot(cache.handle, s.L, s.E), ref.snapshot()):
-            assert np.array_equal(np.asarray(a), np.asarray(b))
-        cache.close()
+    yield pool, shared
     pool.free()
+
+
+@pytest.mark.parametrize("mode", ["full", "qstar"])
+@pytest.mark.parametrize("p", [0.5, 0.8, 0.95])
+def test_qwen_shaped_decode_full_size(ft, wl_mod, qwen_pool, p, mode):
+    """Config at full size (40 x 256 experts, H 2048, I 512, 600 slots, shared expert)
+    at locality p in {0.5, 0.8, 0.95}, full offload (q = m) and q* with B_H = 2 B_P
+    (f = 1/2), in the launch configuration the benchmark times: state on every call,
+    tables at the end, outputs on sampled (step, layer) pairs."""
+    from dataclasses import replace
+    s = replace(wl_mod.SHAPES["qwen_decode"], p=p)
+    pool, shared = qwen_pool
+    steps = 48
+    split = wl_mod.split_tuple(mode, 32768)
+    cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool.ptr, shared=shared, split=split)
+    wl = wl_mod.DecodeWorkload(s, seed=0, steps=steps)
+    ref = SlotCache(s.L, s.E, s.C, full_offload=(mode == "full"), f_q16=32768)
+    for t in range(steps):
+        wl.run_step(cache, t)
+    torch.cuda.synchronize()
+    assert ft.ft_cache_status(cache.handle) == 0
+    experts = oracle_experts(0, s.H, s.I)
+    sample = {(0, 0), (1, 17), (5, 39), (31, 3), (steps - 1, 20)}
+    shared_cache = {}
+    misses = deferred = 0
+    for t in range(steps):
+        for l in range(s.L):
+            r = _check_call(ft, wl, ref, t, l)
+            misses += r.m
+            deferred += r.n_def_routes
+            if (t, l) in sample:
+                if l not in shared_cache:
+                    shared_cache[l] = oracle_shared(0, l, s.H, s.I)
+                _check_output(wl, r, t, l, experts, shared_cache[l])
+    assert misses > 0 and (deferred > 0) == (mode == "qstar")
+    for a, b in zip(ft.ft_cache_snapshot(cache.handle, s.L, s.E), ref.snapshot()):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+    cache.close()
+
+
+def _abs_sum_of_terms(x, ids, gates, layer, E, experts, shared, include):
+    """Per output element, the sum of |term| over the terms the GPU adds into y:
+    |w_j o_j| of its routes and |shared|.  Bounds the reordering error of the sum."""
+    from oracle.moe import swiglu
+    x = np.asarray(x, np.float64)
+    S = np.zeros_like(x)
+    for b in range(ids.shape[0]):
+        for j in range(ids.shape[1]):
+            if include[b, j]:
+                w_gu, w_d = experts(layer * E + int(ids[b, j]))
+                S[b] += np.abs(float(gates[b, j]) * swiglu(w_gu, w_d, x[b:b + 1])[0])
+        if shared is not None:
+            S[b] += np.abs(swiglu(shared[0], shared[1], x[b:b + 1])[0])
+    return S
+
+
+def test_decode_repeat_differs_only_by_summation_order(ft, wl_mod, qwen_pool):
+    """Race check: two caches with the same history make the same calls; the cache
+    state must be identical and y may differ only by the order of its fp32 adds.
+    For n terms summed in two orders the results differ by at most
+    2 (n - 1) u sum|term| (u = 2^-24; checked with 2 n u); a lost, doubled or misplaced term is far larger.
+    Checked on every element of sampled calls against that bound, and on every call
+    against max |y1 - y2| <= 1e-5 rms(y), far below the 5e-3 parity tolerance."""
+    s = wl_mod.SHAPES["qwen_decode"]
+    pool, shared = qwen_pool
+    steps = 8
+    wls, caches = [], []
+    for _ in range(2):
+        caches.append(ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool.ptr, shared=shared))
+        wls.append(wl_mod.DecodeWorkload(s, seed=3, steps=steps))
+    for t in range(steps):
+        for i in range(2):
+            wls[i].run_step(caches[i], t)
+    torch.cuda.synchronize()
+    for name in ("route_slot", "deferred", "counters"):
+        assert torch.equal(getattr(wls[0], name), getattr(wls[1], name)), name
+    y1 = wls[0].y.double().cpu().numpy()
+    y2 = wls[1].y.double().cpu().numpy()
+    d = np.abs(y1 - y2)
+    rms = np.sqrt(np.mean(y1 ** 2, axis=-1, keepdims=True))
+    assert np.all(d <= 1e-5 * rms), f"largest |y1 - y2| / rms {np.max(d / rms):.2e}"
+    experts = oracle_experts(0, s.H, s.I)
+    n_terms = s.k + 1
+    u = 2.0 ** -24
+    for (t, l) in ((0, 0), (3, 21), (steps - 1, s.L - 1)):
+        x = wls[0].x[t, l].float().cpu().numpy()
+        sh = oracle_shared(0, l, s.H, s.I)
+        inc = wls[0].route_slot[t, l].cpu().numpy() >= 0
+        S = _abs_sum_of_terms(x, wls[0].trace[t, l], wls[0].gates[t, l], l, s.E, experts, sh, inc)
+        assert np.all(d[t, l] <= 2 * n_terms * u * S), (t, l)
+    for a, b in zip(ft.ft_cache_snapshot(caches[0].handle, s.L, s.E),
+                    ft.ft_cache_snapshot(caches[1].handle, s.L, s.E)):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+    print("calls with any differing element: %d of %d; largest |y1 - y2| / rms %.2e"
+          % (int(np.any(d > 0, axis=(-1, -2)).sum()), steps * s.L, float(np.max(d / rms))))
+    for c in caches:
+        c.close()
