@@ -22,6 +22,9 @@ Sources:
   [JUHE "Prefill 为什么不能也按需加载"]  the double buffer needs cache_size >= 2 * E.
   [EXPLAINER §7.2]    resize at a safe point: rebuild the GPU cache, keep the host
                       pool, let misses re-warm it.
+  [EXPLAINER §4.3], [JUHE "Prefill 为什么不能也按需加载"]  when the free memory cannot
+                      hold two whole layers the system does not over-allocate: it
+                      falls back to loading on demand.
 
 Readings where the pages are silent (each is listed in the design notes):
   * usage is stamped with a tick that advances once per call (per decode layer
@@ -34,6 +37,11 @@ Readings where the pages are silent (each is listed in the design notes):
     deferred, and the call reports an argument error.
   * a prefill load that finds an expert resident in another slot moves it: the
     old slot becomes free.
+  * on-demand prefill (the fallback) loads the layer's routed union -- every expert
+    some token of the chunk routes to -- through the LRU exactly like decode misses
+    with every miss filled, in groups of at most C experts taken in ascending flat
+    id; each group is one call (one tick; the first group ticks even when the union
+    is empty) and is computed before the next group may evict it.
 """
 from __future__ import annotations
 
@@ -161,6 +169,30 @@ class SlotCache:
             touched |= set(self._load_layer(layer + 1, (layer + 1) % 2))
         self._stamp(touched)
 
+    def prefill_on_demand(self, layer: int, ids) -> list:
+        """On-demand prefill of one layer: the routed union U (ascending flat id) in
+        groups of at most C experts; per group, hits are touched and every miss takes
+        the next least recently used slot that no hit of the group holds.  Returns
+        the groups as lists of (flat id, slot, was_hit) in ascending flat id."""
+        ids = np.asarray(ids, np.int64)
+        E = self.E
+        valid = (ids >= 0) & (ids < E)
+        U = sorted({layer * E + int(e) for e in ids[valid]})
+        groups = [U[i:i + self.C] for i in range(0, len(U), self.C)] or [[]]
+        out = []
+        for grp in groups:
+            self.tick += 1
+            H = [u for u in grp if u in self.slot_for_id]
+            M = [u for u in grp if u not in self.slot_for_id]
+            hit_slots = {self.slot_for_id[u] for u in H}
+            candidates = list(self.free) + [s for s in self.order if s not in hit_slots]
+            victims = candidates[:len(M)]
+            for flat, slot in zip(M, victims):
+                self._map(flat, slot)
+            self._stamp(hit_slots | set(victims))
+            out.append([(u, self.slot_for_id[u], u in H) for u in grp])
+        return out
+
     def _load_layer(self, layer: int, buf: int):
         E = self.E
         slots = range(buf * E, buf * E + E)
@@ -223,6 +255,24 @@ class SlotCacheBruteForce:
         for s in sorted(hit_slots | set(victims)):
             self.history.append((self.tick, s))
         return len(hits), len(misses), q
+
+    def prefill_on_demand(self, layer, ids):
+        """The routed union in groups of at most C, each group a call that fills
+        every miss (re-derived from the touch history, like decode above)."""
+        ids = np.asarray(ids, np.int64)
+        E = self.E
+        wanted = sorted({layer * E + int(e) for e in ids.reshape(-1) if 0 <= e < E})
+        for g0 in range(0, max(len(wanted), 1), self.C):
+            grp = wanted[g0:g0 + self.C]
+            self.tick += 1
+            where = {f: s for s, f in enumerate(self.owner) if f >= 0}
+            hit_slots = {where[f] for f in grp if f in where}
+            misses = [f for f in grp if f not in where]
+            victims = self._lru_order(hit_slots)[:len(misses)]
+            for f, s in zip(misses, victims):
+                self.owner[s] = f
+            for s in sorted(hit_slots | set(victims)):
+                self.history.append((self.tick, s))
 
     def snapshot(self):
         sfi = np.full(self.L * self.E, -1, np.int32)

@@ -134,3 +134,70 @@ def test_resize_empties_and_keeps_counting():
     assert (sfi == -1).all() and ios.tolist() == [-1, -1] and tick == 1
     r = c.decode(0, [[1, 2, 3]])          # cold again; only two slots
     assert (r.m, r.q, r.n_def_routes) == (3, 2, 1) and c.tick == 2
+
+
+# ---------------------------------------------------------------- on-demand prefill
+
+def test_on_demand_prefill_hand_worked():
+    # L = 2, E = 8, C = 3.  Layer 0 decodes experts 0, 1 (slots 0, 1, tick 1); then
+    # layer 1 prefills on demand with the routed union {1, 3, 4, 6, 7} = flats
+    # {9, 11, 12, 14, 15} in groups of three: [9, 11, 12] then [14, 15].
+    c = SlotCache(2, 8, 3)
+    c.decode(0, [[0, 1]])
+    ids = np.array([[1, 3], [4, 1], [6, 7], [3, 6]])
+    groups = c.prefill_on_demand(1, ids)
+    # group 1 (tick 2): no hits; victims in LRU order: free slot 2, then slots 0, 1
+    # (tick 1, by slot) -> 9 -> 2, 11 -> 0 (evicts 0), 12 -> 1 (evicts 1)
+    # group 2 (tick 3): LRU order 0, 1, 2 (all tick 2) -> 14 -> 0, 15 -> 1
+    assert groups == [[(9, 2, False), (11, 0, False), (12, 1, False)],
+                      [(14, 0, False), (15, 1, False)]]
+    sfi, ios, usage, tick = c.snapshot()
+    assert ios.tolist() == [14, 15, 9] and usage.tolist() == [3, 3, 2] and tick == 3
+    assert [int(v) for v in np.nonzero(sfi >= 0)[0]] == [9, 14, 15]
+    # hand-off: decode of layer 1 finds what the prefill left behind
+    r = c.decode(1, [[1, 6]])
+    assert (r.n_hit, r.m, r.q) == (2, 0, 0)
+
+
+def test_on_demand_prefill_hits_stay_and_empty_union_ticks_once():
+    c = SlotCache(1, 8, 4)
+    c.decode(0, [[2, 5]])                                  # 2 -> 0, 5 -> 1 (tick 1)
+    g = c.prefill_on_demand(0, np.array([[5, 7], [2, 7]]))
+    assert g == [[(2, 0, True), (5, 1, True), (7, 2, False)]]       # one group, hits kept
+    assert c.snapshot()[2].tolist() == [2, 2, 2, -1] and c.tick == 2
+    before = c.snapshot()
+    assert c.prefill_on_demand(0, np.array([[-1, 9]])) == [[]]       # masked routes only
+    after = c.snapshot()
+    assert after[3] == before[3] + 1
+    for x, y in zip(after[:3], before[:3]):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_on_demand_prefill_matches_brute_force_history(seed):
+    """Decode calls and on-demand prefill layers interleaved (capacities below, at and
+    above the union size): the OrderedDict model and the history twin agree."""
+    rng = np.random.default_rng(100 + seed)
+    L, E = 3, 16
+    C = int(rng.integers(3, 20))
+    a = SlotCache(L, E, C)
+    b = SlotCacheBruteForce(L, E, C)
+    for it in range(25):
+        l = int(rng.integers(0, L))
+        if it % 3 == 0:
+            T, k = int(rng.integers(1, 12)), 4
+            ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+            groups = a.prefill_on_demand(l, ids)
+            b.prefill_on_demand(l, ids)
+            union = sorted({l * E + int(e) for e in ids.reshape(-1)})
+            assert [f for g in groups for (f, _, _) in g] == union
+            assert all(len(g) <= C for g in groups)
+            # the last group is resident after the call
+            sfi = a.snapshot()[0]
+            assert all(sfi[f] == s for (f, s, _) in groups[-1])
+        else:
+            ids = rng.integers(0, E, (2, 3))
+            r = a.decode(l, ids)
+            assert (r.n_hit, r.m, r.q) == b.decode(l, ids)
+        for x, y in zip(a.snapshot(), b.snapshot()):
+            assert np.array_equal(x, y)
