@@ -728,6 +728,7 @@ def native_prefill(args, ft, wlm, pool, b_p, world):
     assert ft.ft_cache_status(cache.handle) == 0
     cache.close()
     del buf
+    od = prefill_on_demand_leg(args, ft, wlm, pool, b_p, world, xs, routes, y)
     db, db_sp = med_spread(db_ms)
     sb, sb_sp = med_spread(sb_ms)
     cp, cp_sp = med_spread(cp_ms)
@@ -756,6 +757,7 @@ def native_prefill(args, ft, wlm, pool, b_p, world):
                      "copy_only_ms": cp, "copy_only_gbs": streamed / (cp / 1e3) / 1e9,
                      "streamed_bytes": streamed, "b_p_gbs": b_p,
                      "fp4_peak_tflops": fp4_tf, "fp4_peak_source": f"{src} bf16 x 6 (nominal ratio)"},
+        "on_demand": od,
         "gemm": {"gemm1_tflops": g1_flop / (g1_ms / g1_n / 1e3) / 1e12 if g1_n else None,
                  "gemm2_tflops": g2_flop / (g2_ms / g2_n / 1e3) / 1e12 if g2_n else None,
                  "gemm1_ms_per_layer": g1_ms / g1_n if g1_n else None,
@@ -764,6 +766,64 @@ def native_prefill(args, ft, wlm, pool, b_p, world):
                  "copy_ms_per_layer": prof["prefill_copy"][0] / max(prof["prefill_copy"][1], 1),
                  "profiled_chunk": "single-buffered, events around every launch and copy"},
     }
+
+
+def prefill_on_demand_leg(args, ft, wlm, pool, b_p, world, xs, routes, y, capacity=200):
+    """The same chunk with fewer slots than one layer's experts: every layer falls back
+    to loading its routed union on demand, in groups of at most `capacity` experts
+    (the gathers cannot overlap the group's GEMMs).  Bound: the records it fills over
+    the host link at B_P."""
+    import torch
+    s = wlm.SHAPES[args.prefill_workload]
+    T, L = s.T, s.L
+    rec = ft.ft_record_bytes(s.H, s.I)
+    cache = ft.ExpertCache(L, s.E, s.H, s.I, s.k, 1, capacity, pool.ptr, T_max=T)
+    stream = torch.cuda.current_stream()
+
+    def chunk():
+        for l in range(L):
+            ids, gates = routes[l]
+            ft.ft_moe_prefill_layer(cache.handle, l, xs[l], ids, gates, T, s.k, y,
+                                    ft.FT_PREFILL_DOUBLE_BUFFER)
+
+    chunk()
+    torch.cuda.synchronize()
+    ms_all = []
+    for _ in range(2):
+        ft.ft_cache_resize(cache.handle, capacity, cache.slot_buf)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        chunk()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_all.append(max_over_ranks(e0.elapsed_time(e1), world))
+    # fills of one chunk from an emptied cache: every expert of every layer's union is
+    # loaded once per layer (the union covers all experts at this chunk size), so the
+    # streamed bytes are the unions' sizes times the record
+    unions = sum(int(torch.unique(routes[l][0]).numel()) for l in range(L))
+    ft.ft_profile_enable(cache.handle, True)
+    ft.ft_profile_read(cache.handle)
+    ft.ft_cache_resize(cache.handle, capacity, cache.slot_buf)
+    chunk()
+    torch.cuda.synchronize()
+    prof = ft.ft_profile_read(cache.handle)
+    ft.ft_profile_enable(cache.handle, False)
+    assert ft.ft_cache_status(cache.handle) == 0
+    cache.close()
+    ms = statistics.median(ms_all)
+    streamed = unions * rec
+    link_ms = streamed / (b_p * 1e9) * 1e3
+    g_ms, g_n = prof["prefill_copy"]
+    return {"capacity": capacity, "groups_per_layer": (s.E + capacity - 1) // capacity,
+            "ms_per_chunk": ms, "tok_s": T * world / (ms / 1e3), "repeats_ms": [round(v, 2) for v in ms_all],
+            "streamed_bytes": streamed, "link_ms": link_ms, "frac": link_ms / ms,
+            "gather_gbs": streamed / (g_ms / 1e3) / 1e9 if g_ms else None,
+            "gemm1_ms_per_layer": prof["prefill_gemm1"][0] / L, "gemm2_ms_per_layer": prof["prefill_gemm2"][0] / L,
+            "note": "chunk from an emptied cache each time; DOUBLE_BUFFER asked for, 200 < 2E slots: "
+                    "on-demand fallback; gathers and GEMMs of a group run one after the other"}
 
 
 def prefill_only(args, world):

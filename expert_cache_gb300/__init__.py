@@ -21,6 +21,7 @@ FT_DEV_BAD_ID, FT_DEV_TIMEOUT = 0x1, 0x2
 FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR = 0, 1
 FT_PREFILL_DOUBLE_BUFFER = 1
 FT_PREFILL_DEBUG_X = 2
+FT_PREFILL_ON_DEMAND = 4
 FT_PROF_KINDS = 5
 PROF_NAMES = ("decode", "prefill_gemm1", "prefill_gemm2", "prefill_other", "prefill_copy")
 

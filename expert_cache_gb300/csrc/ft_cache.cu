@@ -45,6 +45,11 @@ WsLayout ws_layout(const ft_cache_desc& d) {
         w.pf_h_codes = take(RT * d.I / 2);
         w.pf_h_scales = take(RT * d.I / 16);
         w.pf_o = take(RT * d.H * 4);
+        w.pf_slot_of = take((size_t)d.E * 4);
+        w.pf_gmtile = take((size_t)(d.E + 1) * 4);
+        w.pf_fill_flat = take((size_t)d.E * 4);
+        w.pf_fill_slot = take((size_t)d.E * 4);
+        w.pf_nfill = take(4);
     }
     w.total = off;
     return w;

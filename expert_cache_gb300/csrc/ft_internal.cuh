@@ -86,6 +86,8 @@ struct WsLayout {
     // prefill region (present when T_max > 0)
     size_t pf_chunk_cnt, pf_offsets, pf_mtile, pf_perm, pf_route_pos;
     size_t pf_a_codes, pf_a_scales, pf_h_codes, pf_h_scales, pf_o;
+    // on-demand prefill: per-group expert -> slot, tile prefix and fill list
+    size_t pf_slot_of, pf_gmtile, pf_fill_flat, pf_fill_slot, pf_nfill;
     size_t total;
 };
 

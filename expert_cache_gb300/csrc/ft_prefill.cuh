@@ -35,7 +35,39 @@ struct PrefillArgs {
     uint8_t* debug_h;           // optional: [T*k, I/2] codes then [T*k, I/16] scales, route rows
 };
 
+// On-demand prefill, one group of the layer's routed union (experts with at least
+// one route, ascending) of at most C experts: group g holds union ranks
+// [g*C, g*C + C).  The tables are updated like a decode call that fills every miss.
+struct PrefillDemandArgs {
+    int32_t* slot_for_id;
+    int32_t* id_of_slot;
+    long long* usage;
+    int32_t* lru_order;
+    DevScalars* sc;
+    int C, E, layer, group;
+    const int32_t* offsets;     // [E + 1] sorted-row offsets (from the route sort)
+    int32_t* slot_of;           // [E] out: slot of each expert of the group, else -1
+    int32_t* mtile;             // [E + 1] out: 128-row tile prefix over the group's experts
+    int32_t* fill_flat;         // [E] out: flat id of fill i (ascending)
+    int32_t* fill_slot;         // [E] out: victim slot of fill i
+    int32_t* n_fill;            // out: number of fills
+};
+
+struct PrefillGatherArgs {
+    const uint8_t* host_pool;   // device-mapped pinned pool
+    uint8_t* slot_buf;
+    size_t rec_bytes;
+    const int32_t* fill_flat;
+    const int32_t* fill_slot;
+    const int32_t* n_fill;
+};
+
 cudaError_t launch_pf_tables(const PrefillTablesArgs& a, cudaStream_t s);
+// bytes (a multiple of 16, both ends 16-byte aligned) from src (device-mapped pinned
+// host memory) to dst (device).
+cudaError_t launch_pf_stream(const void* src, void* dst, size_t bytes, cudaStream_t s);
+cudaError_t launch_pf_demand_tables(const PrefillDemandArgs& a, cudaStream_t s);
+cudaError_t launch_pf_gather(const PrefillGatherArgs& a, cudaStream_t s);
 cudaError_t launch_pf_sort_quant(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_pf_combine(const PrefillArgs& a, cudaStream_t s);
 

@@ -95,6 +95,191 @@ __global__ void __launch_bounds__(1024, 1) pf_tables_kernel(PrefillTablesArgs a)
     }
 }
 
+// ------------------------------------------------------------------ on-demand tables
+// One CTA of 1024 threads per group.  Expert e belongs to thread e / ne (ne experts
+// per thread, contiguous) and slot position p to thread p / nc, so block scans run
+// in ascending expert id and ascending LRU position.
+__global__ void __launch_bounds__(1024, 1) pf_demand_tables_kernel(PrefillDemandArgs a) {
+    __shared__ int s_scan[33];
+    __shared__ uint32_t s_hit[kMaxC / 32];        // slots held by a hit of this group
+    __shared__ uint32_t s_touch[kMaxC / 32];      // hits and victims
+    const int tid = threadIdx.x, E = a.E, C = a.C;
+    const int ne = (E + 1023) / 1024, nc = (C + 1023) / 1024, nw = (C + 31) / 32;
+    for (int w = tid; w < nw; w += 1024) { s_hit[w] = 0; s_touch[w] = 0; }
+    // ---- union rank of every routed expert; group membership
+    int used[kExpertsPerThread];
+    int n_used = 0;
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        const int e = tid * ne + j;
+        used[j] = (j < ne && e < E && a.offsets[e + 1] > a.offsets[e]) ? 1 : 0;
+        n_used += used[j];
+    }
+    int U = 0;
+    int rank = block_exclusive_scan(n_used, &U, s_scan);
+    const int g0 = a.group * C;
+    const int n_members = min(C, U - g0);
+    int member[kExpertsPerThread], slot[kExpertsPerThread];
+    int n_miss = 0;
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        member[j] = used[j] && rank >= g0 && rank < g0 + C;
+        rank += used[j];
+        slot[j] = -1;
+        if (member[j]) {
+            const int e = tid * ne + j;
+            slot[j] = a.slot_for_id[a.layer * E + e];
+            if (slot[j] >= 0) atomicOr(&s_hit[slot[j] >> 5], 1u << (slot[j] & 31));
+            else ++n_miss;
+        }
+    }
+    if (n_members <= 0) {                          // nothing in this group
+#pragma unroll
+        for (int j = 0; j < kExpertsPerThread; ++j) {
+            const int e = tid * ne + j;
+            if (j < ne && e < E) { a.slot_of[e] = -1; a.mtile[e] = 0; }
+        }
+        if (tid == 0) {
+            a.mtile[E] = 0;
+            *a.n_fill = 0;
+            if (a.group == 0) a.sc->tick = a.sc->tick + 1;   // the call still ticks once
+        }
+        return;
+    }
+    int m = 0;
+    int miss_rank = block_exclusive_scan(n_miss, &m, s_scan);   // also orders s_hit
+    const long long tick = a.sc->tick + 1;
+    // ---- victims: the first m entries of the LRU order that no hit holds
+    int ent[kSlotsPerThread];
+    int n_keep = 0;
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        const int pos = tid * nc + j;
+        ent[j] = (j < nc && pos < C) ? a.lru_order[pos] : -1;
+        if (ent[j] >= 0 && !((s_hit[ent[j] >> 5] >> (ent[j] & 31)) & 1u)) ++n_keep;
+    }
+    int vrank = block_exclusive_scan(n_keep, nullptr, s_scan);
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        if (ent[j] >= 0 && !((s_hit[ent[j] >> 5] >> (ent[j] & 31)) & 1u)) {
+            if (vrank < m) a.fill_slot[vrank] = ent[j];
+            ++vrank;
+        }
+    }
+    __syncthreads();                               // fill_slot complete (same CTA)
+    // ---- misses take their victims in ascending expert id; evicted ids unmapped
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        const int e = tid * ne + j;
+        if (member[j] && slot[j] < 0) {
+            const int v = a.fill_slot[miss_rank];
+            const int flat = a.layer * E + e;
+            const int old = a.id_of_slot[v];
+            if (old >= 0) a.slot_for_id[old] = -1;
+            a.slot_for_id[flat] = v;
+            a.id_of_slot[v] = flat;
+            a.fill_flat[miss_rank] = flat;
+            slot[j] = v;
+            ++miss_rank;
+        }
+        if (j < ne && e < E) a.slot_of[e] = member[j] ? slot[j] : -1;
+        if (member[j]) atomicOr(&s_touch[slot[j] >> 5], 1u << (slot[j] & 31));
+    }
+    // ---- 128-row tile prefix over the group's experts
+    int tiles = 0;
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        const int e = tid * ne + j;
+        if (member[j]) tiles += (a.offsets[e + 1] - a.offsets[e] + 127) / 128;
+    }
+    int all_tiles = 0;
+    int toff = block_exclusive_scan(tiles, &all_tiles, s_scan);   // also orders s_touch
+#pragma unroll
+    for (int j = 0; j < kExpertsPerThread; ++j) {
+        const int e = tid * ne + j;
+        if (j < ne && e < E) {
+            a.mtile[e] = toff;
+            if (member[j]) toff += (a.offsets[e + 1] - a.offsets[e] + 127) / 128;
+        }
+    }
+    if (tid == 0) { a.mtile[E] = all_tiles; *a.n_fill = m; }
+    // ---- LRU order: untouched slots keep their order, touched ones follow ascending
+    int n_untouched = 0;
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j)
+        if (ent[j] >= 0 && !((s_touch[ent[j] >> 5] >> (ent[j] & 31)) & 1u)) ++n_untouched;
+    int tot_untouched = 0;
+    int r_keep = block_exclusive_scan(n_untouched, &tot_untouched, s_scan);   // every ent[] read
+    int n_t = 0;
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        const int sl = tid * nc + j;
+        if (j < nc && sl < C && ((s_touch[sl >> 5] >> (sl & 31)) & 1u)) ++n_t;
+    }
+    int r_touch = block_exclusive_scan(n_t, nullptr, s_scan);
+#pragma unroll
+    for (int j = 0; j < kSlotsPerThread; ++j) {
+        if (ent[j] >= 0 && !((s_touch[ent[j] >> 5] >> (ent[j] & 31)) & 1u)) a.lru_order[r_keep++] = ent[j];
+        const int sl = tid * nc + j;
+        if (j < nc && sl < C && ((s_touch[sl >> 5] >> (sl & 31)) & 1u)) {
+            a.lru_order[tot_untouched + r_touch++] = sl;
+            a.usage[sl] = tick;
+        }
+    }
+    if (tid == 0) a.sc->tick = tick;
+}
+
+// Fill records of one on-demand group: pinned pool -> victim slots, 16-byte pieces
+// read over the host link by every thread of the grid, four in flight per thread.
+__global__ void pf_gather_kernel(PrefillGatherArgs a) {
+    const int n = *a.n_fill;
+    const size_t per = a.rec_bytes / 16;
+    const size_t total = (size_t)n * per;
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; i0 < total; i0 += stride) {
+        uint4 v[4];
+        size_t dst[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const size_t i = i0 + (size_t)j * blockDim.x;
+            if (i < total) {
+                const size_t r = i / per, off = (i % per) * 16;
+                v[j] = *reinterpret_cast<const uint4*>(a.host_pool + (size_t)a.fill_flat[r] * a.rec_bytes + off);
+                dst[j] = (size_t)a.fill_slot[r] * a.rec_bytes + off;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const size_t i = i0 + (size_t)j * blockDim.x;
+            if (i < total) *reinterpret_cast<uint4*>(a.slot_buf + dst[j]) = v[j];
+        }
+    }
+}
+
+// Whole-layer stream-in: n16 16-byte pieces from the device-mapped pinned pool to
+// the buffer, read over the host link by SM loads (eight in flight per thread,
+// coalesced per warp), on the cache's copy stream next to the compute stream's
+// GEMMs.  SM loads reach the link's rate whichever copy engine a stream is given.
+// A quarter of the SMs (one CTA each, about 1.2 MB in flight) keep the link busy;
+// two CTAs on every SM kept it busy too but slowed the GEMMs beside them 2.5-fold.
+__global__ void __launch_bounds__(256) pf_stream_kernel(const uint4* __restrict__ src,
+                                                        uint4* __restrict__ dst, size_t n16) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 8;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x * 8 + threadIdx.x; i0 < n16; i0 += stride) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const size_t i = i0 + (size_t)j * blockDim.x;
+            if (i < n16) v[j] = __ldcs(src + i);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const size_t i = i0 + (size_t)j * blockDim.x;
+            if (i < n16) dst[i] = v[j];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ route sort
 // Chunks of 32 tokens.  Count of routes per (chunk, expert); a route with an id
 // outside [0, E) or repeating an id of its own token is masked (status bit).
@@ -238,6 +423,22 @@ __global__ void pf_combine_kernel(PrefillArgs a) {
 
 cudaError_t launch_pf_tables(const PrefillTablesArgs& a, cudaStream_t s) {
     pf_tables_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_stream(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+    pf_stream_kernel<<<(sm_count() + 3) / 4, 256, 0, s>>>(static_cast<const uint4*>(src),
+                                                      static_cast<uint4*>(dst), bytes / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_demand_tables(const PrefillDemandArgs& a, cudaStream_t s) {
+    pf_demand_tables_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_gather(const PrefillGatherArgs& a, cudaStream_t s) {
+    pf_gather_kernel<<<sm_count() * 4, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

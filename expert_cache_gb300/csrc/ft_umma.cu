@@ -177,7 +177,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             const TileInfo ti = tile_info(g, tile);
-            const int slot = g.slot0 + ti.e;
+            const int slot = g.slot_of ? g.slot_of[ti.e] : g.slot0 + ti.e;
             const uint8_t* rec = g.slot_buf + (size_t)slot * g.rec_bytes;
             for (int ks = 0; ks < kstages; ++ks, ++it) {
                 const int s = it % kStages;
@@ -288,7 +288,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const bool valid = r < ti.rows;
             const int p = ti.m0 + r;
             const int route = valid ? g.perm[p] : 0;
-            const uint8_t* rec = g.slot_buf + (size_t)(g.slot0 + ti.e) * g.rec_bytes;
+            const uint8_t* rec = g.slot_buf + (size_t)(g.slot_of ? g.slot_of[ti.e] : g.slot0 + ti.e) * g.rec_bytes;
             const float ts = *reinterpret_cast<const float*>(rec + g.off_tscale);
             if (g.kind == 1) {
                 for (int c = 0; c < 128; c += 16) {

@@ -11,7 +11,8 @@ struct UmmaArgs {
     int n_tiles_n;              // 256-column tiles per expert
     int R_max, R_total;         // rows of the sorted buffers, valid routes T*k
     int I, H;
-    int slot0;                  // slot of expert 0 of the layer (buffer base)
+    int slot0;                  // slot of expert 0 of the layer (buffer base) ...
+    const int32_t* slot_of;     // ... or, when not null, the slot of each expert
     const uint8_t* slot_buf;
     size_t rec_bytes;
     size_t off_b_scales;        // record offset of the B scales (W_gu or W_d)

@@ -174,11 +174,18 @@ ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
                                int32_t* counters, void* stream);
 
 /* Prefill of one layer over a T-token chunk ([EXPLAINER §4.1-4.3]; [JUHE "Prefill 为什么
- * 不能也按需加载"]).  With FT_PREFILL_DOUBLE_BUFFER the layer's experts sit in buffer
- * (layer mod 2) = slots [(layer%2)*E, +E) and, while this layer computes, every
- * expert of layer+1 streams into the other buffer on the internal copy stream;
- * capacity must be >= 2E (else FT_ERR_CAPACITY).  Without it only buffer 0 is used
- * and each layer is loaded before it computes.  Activations and h are NVFP4 (unit
+ * 不能也按需加载"]).  With FT_PREFILL_DOUBLE_BUFFER and capacity >= 2E the layer's
+ * experts sit in buffer (layer mod 2) = slots [(layer%2)*E, +E) and, while this layer
+ * computes, every expert of layer+1 streams into the other buffer on the internal copy
+ * stream.  Without the flag and with capacity >= E only buffer 0 is used and each
+ * layer is loaded before it computes.  Otherwise (two layers do not fit for the double
+ * buffer, one does not fit for the single one) or with FT_PREFILL_ON_DEMAND, the call
+ * falls back to loading on demand: the layer's routed union (experts with at least one
+ * valid route, ascending id) goes through the global LRU like decode misses with every
+ * miss filled, in groups of at most C experts (one tick per group, the first group
+ * ticks even for an empty union); each group's missing records are streamed from the
+ * pinned pool into their victim slots by the GPU and the group is computed before the
+ * next one may evict it.  What is resident afterwards is decode's cache.  Activations and h are NVFP4 (unit
  * tensor scale, E4M3 per 16); the two grouped GEMMs run on tcgen05 block-scaled
  * FP4 tensor cores; y[t] = sum_j w[t,j] * o_(t,j) in order j.
  *   x         device bf16 [T, H];  topk_ids device int32 [T, k];  topk_w device fp32 [T, k]
@@ -190,9 +197,15 @@ ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
  *             route), then [T*k, H/2] packed x codes and [T*k, H/16] x scales in
  *             sorted-row order (rows past the last valid route are unspecified).
  *             Total bytes: T*k*(I/2 + I/16 + 4 + H/2 + H/16).
- * Calls for one chunk go layer 0, 1, ..., L-1 on the same stream. */
+ * Calls for one chunk go layer 0, 1, ..., L-1 on the same stream.
+ * Errors (host-side, nothing launched): FT_ERR_STATE when the cache was created with
+ * T_max = 0; FT_ERR_ARG for H or I not multiples of 256, layer outside [0, L), T
+ * outside [1, T_max], k outside [1, k_max], NULL x/ids/w/y, x or y not 16-byte
+ * aligned, or an unknown flag.  Route ids outside [0, E), or repeating an id of their
+ * own token, mask the route and set FT_DEV_BAD_ID. */
 #define FT_PREFILL_DOUBLE_BUFFER 1
 #define FT_PREFILL_DEBUG_X       2
+#define FT_PREFILL_ON_DEMAND     4
 ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t T,
                                int32_t k, float* y, int32_t flags, void* debug_h,

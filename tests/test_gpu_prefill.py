@@ -136,12 +136,15 @@ def _check_x(x_f32, k, pos, xc_packed, xs, routes=None):
     return len(r)
 
 
-def _run_chunk(ft, wl_mod, L, E, H, I, k, T, C, db, seed, check_state=True, layers=None):
+def _run_chunk(ft, wl_mod, L, E, H, I, k, T, C, db, seed, check_state=True, layers=None,
+               on_demand=False, extra_flags=0):
+    """One chunk through L layers; db: ask for the double buffer; on_demand: the
+    oracle state follows the on-demand fallback (routed union through the LRU)."""
     pool = wl_mod.build_pool(seed, L, E, H, I)
     cache = ft.ExpertCache(L, E, H, I, k, 1, C, pool.ptr, T_max=T)
     ref = SlotCache(L, E, C)
     experts = oracle_experts(seed, H, I)
-    flags = (ft.FT_PREFILL_DOUBLE_BUFFER if db else 0) | ft.FT_PREFILL_DEBUG_X
+    flags = (ft.FT_PREFILL_DOUBLE_BUFFER if db else 0) | ft.FT_PREFILL_DEBUG_X | extra_flags
     R = T * k
     dbg = torch.empty(_debug_bytes(R, I, H, True), dtype=torch.uint8, device="cuda")
     y = torch.empty((T, H), dtype=torch.float32, device="cuda")
@@ -151,7 +154,10 @@ def _run_chunk(ft, wl_mod, L, E, H, I, k, T, C, db, seed, check_state=True, laye
         ft.ft_moe_prefill_layer(cache.handle, l, x, ids, gates, T, k, y, flags, dbg)
         torch.cuda.synchronize()
         assert ft.ft_cache_status(cache.handle) == 0
-        ref.prefill(l, db)
+        if on_demand:
+            ref.prefill_on_demand(l, ids.cpu().numpy())
+        else:
+            ref.prefill(l, db)
         if check_state:
             for a_, b_ in zip(ft.ft_cache_snapshot(cache.handle, L, E), ref.snapshot()):
                 assert np.array_equal(np.asarray(a_), np.asarray(b_)), f"layer {l}"
@@ -165,6 +171,22 @@ def _run_chunk(ft, wl_mod, L, E, H, I, k, T, C, db, seed, check_state=True, laye
         y_gpu = y.cpu().numpy()
         assert_close(y_gpu, prefill_from_h(gc, gs, idn, gn, l, E, experts), f"stage 2, layer {l}")
         assert_close(y_gpu, y_or, f"end to end, layer {l}")
+    # hand-off: decode continues from what prefill left resident
+    if on_demand or check_state:
+        rng = np.random.default_rng(seed)
+        for call in range(6):
+            l = call % L
+            ids_d = np.stack([rng.choice(E, k, replace=False)]).astype(np.int32)
+            xd = synth.decode_x(seed, call, l, L, 1, H, "cuda")
+            yd = torch.empty((1, H), device="cuda")
+            dd = torch.empty((1, k), dtype=torch.int32, device="cuda")
+            ct = torch.empty(4, dtype=torch.int32, device="cuda")
+            ft.ft_moe_decode(cache.handle, l, xd, torch.from_numpy(ids_d).cuda(),
+                             torch.full((1, k), 1.0 / k, device="cuda"), 1, k, yd, dd, None, ct)
+            r = ref.decode(l, ids_d)
+            assert ct.cpu().tolist() == [r.n_hit, r.m, r.q, r.n_def_routes], f"decode call {call}"
+        for a_, b_ in zip(ft.ft_cache_snapshot(cache.handle, L, E), ref.snapshot()):
+            assert np.array_equal(np.asarray(a_), np.asarray(b_)), "tables after the hand-off"
     cache.close()
     pool.free()
 
@@ -186,21 +208,40 @@ def test_prefill_wider_shapes(ft, wl_mod):
     _run_chunk(ft, wl_mod, L=2, E=16, H=1024, I=512, k=4, T=300, C=40, db=True, seed=4)
 
 
-def test_prefill_capacity_errors(ft, wl_mod):
+def test_prefill_argument_errors(ft, wl_mod):
     L, E, H, I, k, T = 2, 8, 256, 256, 2, 16
     pool = wl_mod.build_pool(5, L, E, H, I)
     cache = ft.ExpertCache(L, E, H, I, k, 1, 12, pool.ptr, T_max=T)
     x = synth.prefill_x(5, 0, T, H, "cuda")
     ids, gates = synth.prefill_routes(5, 0, T, E, k, "cuda")
     y = torch.empty((T, H), device="cuda")
-    with pytest.raises(ft.FtError) as ei:
-        ft.ft_moe_prefill_layer(cache.handle, 0, x, ids, gates, T, k, y, ft.FT_PREFILL_DOUBLE_BUFFER)
-    assert ei.value.status == ft.FT_ERR_CAPACITY
-    with pytest.raises(ft.FtError) as ei:
-        ft.ft_moe_prefill_layer(cache.handle, 0, x, ids, gates, T + 1, k, y, 0)
-    assert ei.value.status == ft.FT_ERR_ARG
+    for bad in (dict(T=T + 1), dict(flags=64), dict(layer=L), dict(k=k + 1)):
+        kw = dict(layer=0, T=T, k=k, flags=0)
+        kw.update(bad)
+        with pytest.raises(ft.FtError) as ei:
+            ft.ft_moe_prefill_layer(cache.handle, kw["layer"], x, ids, gates, kw["T"], kw["k"], y,
+                                    kw["flags"])
+        assert ei.value.status == ft.FT_ERR_ARG, bad
     cache.close()
     pool.free()
+
+
+@pytest.mark.parametrize("C,flags", [(6, 0), (12, 1), (20, 1), (40, 4)])
+def test_prefill_on_demand_fallback(ft, wl_mod, C, flags):
+    """Capacity below two layers (with the double buffer asked for) or below one
+    layer: the call falls back to the routed union on demand; C = 6 takes three
+    groups per layer, 12 two, 20 one; C = 40 asks for the on-demand path directly.
+    Tables after every layer, x, h and y as in the whole-layer path, then decode
+    from what the prefill left resident."""
+    _run_chunk(ft, wl_mod, L=3, E=16, H=256, I=256, k=4, T=200, C=C,
+               db=bool(flags & 1), seed=7, on_demand=True, extra_flags=flags & 4)
+
+
+def test_prefill_on_demand_sparse_union(ft, wl_mod):
+    """A short chunk routes to few experts: only the union is loaded (hits from the
+    previous layers' calls stay), one group."""
+    _run_chunk(ft, wl_mod, L=4, E=64, H=256, I=256, k=2, T=5, C=24, db=False, seed=8,
+               on_demand=True, extra_flags=4)
 
 
 def test_prefill_then_decode_hands_over_the_buffers(ft, wl_mod):
@@ -324,4 +365,44 @@ def test_prefill_qwen_shaped_full_chunk(ft, wl_mod, qwen_prefill_pool):
     assert np.array_equal(sfi[L - 2], (L - 2) % 2 * E + np.arange(E))
     assert np.all(sfi[:L - 2] == -1)
     print("h flips (codes, scales, worst midpoint distance) per checked layer:", flips)
+    cache.close()
+
+
+def test_prefill_qwen_shaped_on_demand(ft, wl_mod, qwen_prefill_pool):
+    """The Qwen-shaped 8192-token chunk with 200 slots (fewer than one layer's 256
+    experts): every layer falls back to on-demand loading in two groups.  Tables
+    after every layer; x, h and y on sampled tokens of two layers."""
+    from expert_cache_gb300.workloads import SHAPES
+    s = SHAPES["qwen_prefill"]
+    L, T, E, H, I, k, C = 6, s.T, s.E, s.H, s.I, s.k, 200
+    cache = ft.ExpertCache(L, E, H, I, k, 1, C, qwen_prefill_pool.ptr, T_max=T)
+    ref = SlotCache(L, E, C)
+    experts = oracle_experts(0, H, I)
+    R = T * k
+    dbg = torch.empty(_debug_bytes(R, I, H, True), dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, H), device="cuda")
+    rows = np.array([3, 2048, T - 2])
+    routes = (rows[:, None] * k + np.arange(k)).reshape(-1)
+    for l in range(L):
+        x = synth.prefill_x(0, l, T, H, "cuda")
+        ids, gates = synth.prefill_routes(0, l, T, E, k, "cuda")
+        checked = l in (0, L - 1)
+        flags = ft.FT_PREFILL_DOUBLE_BUFFER | (ft.FT_PREFILL_DEBUG_X if checked else 0)
+        ft.ft_moe_prefill_layer(cache.handle, l, x, ids, gates, T, k, y, flags, dbg if checked else None)
+        groups = ref.prefill_on_demand(l, ids.cpu().numpy())
+        assert len(groups) == 2
+        for a_, b_ in zip(ft.ft_cache_snapshot(cache.handle, L, E), ref.snapshot()):
+            assert np.array_equal(np.asarray(a_), np.asarray(b_)), f"tables after layer {l}"
+        assert ft.ft_cache_status(cache.handle) == 0
+        if not checked:
+            continue
+        xn, idn, gn = x.float().cpu().numpy(), ids.cpu().numpy(), gates.cpu().numpy()
+        gc, gs, pos, xc, xs = _split_debug(dbg.cpu().numpy(), R, I, H)
+        assert _check_x(xn, k, pos, xc, xs, routes) == len(routes)
+        y_or, oc, os_, h32 = prefill_layer(xn[rows], idn[rows], gn[rows], l, E, experts, return_h32=True)
+        _check_h(gc[routes], gs[routes], oc, os_, h32, np.ones(len(routes), bool))
+        y_rows = y.cpu().numpy()[rows]
+        assert_close(y_rows, prefill_from_h(gc[routes], gs[routes], idn[rows], gn[rows], l, E, experts),
+                     f"stage 2, layer {l}")
+        assert_close(y_rows, y_or, f"end to end, layer {l}")
     cache.close()
