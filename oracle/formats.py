@@ -19,6 +19,15 @@ Record layout (bytes, one per flat id, padded to a multiple of 256):
   Two codes per byte, element 2j in the low nibble, element 2j+1 in the high one.
   Scales are unsigned E4M3 bytes, row-major [rows, K/16].
 
+MXFP4 ([EXPLAINER §9.2] and the model table: DeepSeek-V4-Flash's routed experts are
+natively MXFP4, and the engines consume those blocks bit-exactly): E2M1 codes as above,
+one unsigned E8M0 scale (value 2^(c - 127), code 255 is NaN) per 32 consecutive
+elements of a row, no tensor scale.  The MXFP4 record has the same layout with the
+scale arrays [rows, K/32] and the two tensor-scale words fixed at 1.0.  Synthetic
+MXFP4 pools are quantised with the conversion rule of the microscaling format
+definition: shared exponent floor(log2(amax_32)) - 2 (2 = the largest E2M1
+exponent), clamped to [-127, 127]; code = E2M1_RNE_sat(v / 2^shared).
+
 Quantiser arithmetic is written as fp32 IEEE round-to-nearest steps (numpy float32
 ops), so that a device implementation doing the same fp32 steps is bit-exact.
 Decoding goes to fp64 and is exact.
@@ -104,6 +113,15 @@ def e4m3_encode_unsigned(v) -> np.ndarray:
     return _nearest_even(v, _E4M3_POS).astype(np.uint8)
 
 
+# ---------------------------------------------------------------- E8M0 (MX scale)
+
+def e8m0_decode(codes) -> np.ndarray:
+    """Value of unsigned 8-bit E8M0 scale codes: 2^(c - 127); code 255 is NaN."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    v = np.ldexp(1.0, c - 127)
+    return np.where(c == 255, np.nan, v).astype(np.float64)
+
+
 # ---------------------------------------------------------------- quantisers
 
 F32 = np.float32
@@ -158,6 +176,39 @@ def quantize_act(x) -> tuple[np.ndarray, np.ndarray]:
     return e2m1_encode(qv).reshape(rows, k), sc
 
 
+MX_BLOCK = 32
+
+
+def quantize_mx(w) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4 quantiser (conversion rule of the microscaling format definition), fp32
+    IEEE steps, per 32 consecutive elements of a row:
+      shared = floor(log2(amax)) - 2, clamped to [-127, 127] (amax = 0: -127);
+      scale code = shared + 127;  code = E2M1_RNE_sat(v * 2^-shared).
+    floor(log2(amax)) is exact: the exponent of amax's binary representation.
+    Returns (codes uint8 [rows, K] one code per element, scales uint8 [rows, K/32])."""
+    w = np.asarray(w, dtype=F32)
+    rows, k = w.shape
+    assert k % MX_BLOCK == 0
+    blocks = w.reshape(rows, k // MX_BLOCK, MX_BLOCK)
+    amax = np.max(np.abs(blocks), axis=2).astype(F32)
+    _, e = np.frexp(amax)                       # amax = m * 2^e, m in [0.5, 1)
+    shared = np.where(amax > 0, e.astype(np.int64) - 1 - 2, -127)
+    shared = np.clip(shared, -127, 127)
+    mul = np.ldexp(np.float32(1.0), (-shared).astype(np.int32)).astype(F32)   # exact powers of two
+    qv = (blocks * mul[..., None]).astype(F32)
+    codes = e2m1_encode(qv).reshape(rows, k)
+    return codes, (shared + 127).astype(np.uint8)
+
+
+def dequant_mx(codes, scales) -> np.ndarray:
+    """fp64 value of MXFP4 data: e2m1(code) * 2^(scale - 127) of its 32-block (exact)."""
+    codes = np.asarray(codes)
+    rows, k = codes.shape
+    v = e2m1_decode(codes).reshape(rows, k // MX_BLOCK, MX_BLOCK)
+    v = v * e8m0_decode(scales)[..., None]
+    return v.reshape(rows, k)
+
+
 def dequant(codes, scales, s_t=1.0) -> np.ndarray:
     """fp64 value of NVFP4 data: e2m1(code) * e4m3(scale of its 16-block) * s_t (exact)."""
     codes = np.asarray(codes)
@@ -183,13 +234,17 @@ def unpack_nibbles(packed) -> np.ndarray:
     return out
 
 
-def record_layout(H: int, I: int) -> dict:
+FORMATS = ("nvfp4", "mxfp4")
+
+
+def record_layout(H: int, I: int, fmt: str = "nvfp4") -> dict:
     """Byte offsets and sizes of one expert record for hidden H, intermediate I."""
-    assert H % BLOCK == 0 and I % BLOCK == 0
+    sb = BLOCK if fmt == "nvfp4" else MX_BLOCK
+    assert fmt in FORMATS and H % sb == 0 and I % sb == 0
     lay = {}
     off = 0
-    for name, size in (("gu_codes", 2 * I * H // 2), ("gu_scales", 2 * I * H // BLOCK),
-                       ("d_codes", H * I // 2), ("d_scales", H * I // BLOCK),
+    for name, size in (("gu_codes", 2 * I * H // 2), ("gu_scales", 2 * I * H // sb),
+                       ("d_codes", H * I // 2), ("d_scales", H * I // sb),
                        ("s_gu", 4), ("s_d", 4)):
         lay[name] = (off, size)
         off += size
@@ -198,15 +253,22 @@ def record_layout(H: int, I: int) -> dict:
     return lay
 
 
-def encode_record(w_gu, w_d) -> np.ndarray:
+def encode_record(w_gu, w_d, fmt: str = "nvfp4") -> np.ndarray:
     """Quantise fp32 W_gu [2I, H] and W_d [H, I] into one padded record (uint8)."""
     w_gu = np.asarray(w_gu, F32)
     w_d = np.asarray(w_d, F32)
     two_i, H = w_gu.shape
     I = two_i // 2
     assert w_d.shape == (H, I)
-    lay = record_layout(H, I)
+    lay = record_layout(H, I, fmt)
     rec = np.zeros(lay["bytes"], np.uint8)
+    if fmt == "mxfp4":
+        for w, cn, sn, tn in ((w_gu, "gu_codes", "gu_scales", "s_gu"), (w_d, "d_codes", "d_scales", "s_d")):
+            c, sc = quantize_mx(w)
+            _put(rec, lay[cn], pack_nibbles(c))
+            _put(rec, lay[sn], sc)
+            _put(rec, lay[tn], np.array([1.0], F32).view(np.uint8))
+        return rec
     c, s, t = quantize_weight(w_gu)
     _put(rec, lay["gu_codes"], pack_nibbles(c))
     _put(rec, lay["gu_scales"], s)
@@ -230,22 +292,25 @@ def _get(rec, where):
     return np.asarray(rec[off:off + size], np.uint8)
 
 
-def record_fields(rec, H: int, I: int) -> dict:
+def record_fields(rec, H: int, I: int, fmt: str = "nvfp4") -> dict:
     """Split a record into its raw fields (codes unpacked, scales, tensor scales)."""
-    lay = record_layout(H, I)
+    lay = record_layout(H, I, fmt)
+    sb = BLOCK if fmt == "nvfp4" else MX_BLOCK
     rec = np.asarray(rec, np.uint8)
     return {
         "gu_codes": unpack_nibbles(_get(rec, lay["gu_codes"]).reshape(2 * I, H // 2)),
-        "gu_scales": _get(rec, lay["gu_scales"]).reshape(2 * I, H // BLOCK),
+        "gu_scales": _get(rec, lay["gu_scales"]).reshape(2 * I, H // sb),
         "d_codes": unpack_nibbles(_get(rec, lay["d_codes"]).reshape(H, I // 2)),
-        "d_scales": _get(rec, lay["d_scales"]).reshape(H, I // BLOCK),
+        "d_scales": _get(rec, lay["d_scales"]).reshape(H, I // sb),
         "s_gu": _get(rec, lay["s_gu"]).view(F32)[0],
         "s_d": _get(rec, lay["s_d"]).view(F32)[0],
     }
 
 
-def decode_record(rec, H: int, I: int) -> tuple[np.ndarray, np.ndarray]:
+def decode_record(rec, H: int, I: int, fmt: str = "nvfp4") -> tuple[np.ndarray, np.ndarray]:
     """fp64 (W_gu [2I, H], W_d [H, I]) of a record."""
-    f = record_fields(rec, H, I)
+    f = record_fields(rec, H, I, fmt)
+    if fmt == "mxfp4":
+        return dequant_mx(f["gu_codes"], f["gu_scales"]), dequant_mx(f["d_codes"], f["d_scales"])
     return (dequant(f["gu_codes"], f["gu_scales"], f["s_gu"]),
             dequant(f["d_codes"], f["d_scales"], f["s_d"]))

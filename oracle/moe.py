@@ -39,15 +39,16 @@ def swiglu(w_gu: np.ndarray, w_d: np.ndarray, x: np.ndarray) -> np.ndarray:
 
 
 class RecordSource:
-    """Decoded-expert lookup with a small memo, from a callable flat_id -> record bytes."""
+    """Decoded-expert lookup with a small memo, from a callable flat_id -> record bytes
+    (records in format fmt: "nvfp4" or "mxfp4")."""
 
-    def __init__(self, get_record, H: int, I: int):
-        self.get_record, self.H, self.I = get_record, H, I
+    def __init__(self, get_record, H: int, I: int, fmt: str = "nvfp4"):
+        self.get_record, self.H, self.I, self.fmt = get_record, H, I, fmt
         self.memo = {}
 
     def __call__(self, flat: int):
         if flat not in self.memo:
-            self.memo[flat] = decode_record(self.get_record(flat), self.H, self.I)
+            self.memo[flat] = decode_record(self.get_record(flat), self.H, self.I, self.fmt)
         return self.memo[flat]
 
 

@@ -153,3 +153,125 @@ def test_pool_shape_matches_pages_bf16_pool():
     assert abs(pool_bf16 / 1e9 - float(gb)) < 0.05
     t = pool_bf16 / (float(bp) * 1e9)
     assert float(lo) <= t + 0.01 and t <= float(hi) + 0.01
+
+
+# ---------------------------------------------------------------- MXFP4
+
+def test_e8m0_decode_matches_torch_float8_e8m0():
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without float8_e8m0fnu")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = F.e8m0_decode(codes)
+    assert np.isnan(got[255]) and np.isnan(ref[255])
+    assert np.array_equal(got[:255], ref[:255])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+
+
+def _brute_mx_block(v):
+    """Shared exponent k with 2^(k+2) <= amax < 2^(k+3) found by search, and each code
+    as the nearest of the 16 E2M1 values to v / 2^k (ties to the even code, beyond 6
+    the largest)."""
+    import math
+    a = max(abs(float(x)) for x in v)
+    if a == 0:
+        k = -127
+    else:
+        k = -200
+        while 2.0 ** (k + 3) <= a:
+            k += 1
+        k = max(-127, min(127, k))
+    codes = []
+    for x in v:
+        t = float(x) / 2.0 ** k
+        best = None
+        for c in range(16):
+            val = F.e2m1_decode(c)
+            d = abs(float(val) - t)
+            key = (d, c & 1, c)                 # nearest; ties: even mantissa bit
+            if abs(t) > 6:
+                key = (abs(abs(float(val)) - 6) + (0 if (val < 0) == (t < 0) else 9), 0, c)
+            if best is None or key < best[0]:
+                best = (key, c)
+        c = best[1]
+        if float(F.e2m1_decode(c)) == 0:
+            c = 0                               # zero magnitudes are +0
+        codes.append(c)
+    return k + 127, codes
+
+
+def test_quantize_mx_constructions():
+    grid = [6.0, 4.0, -3.0, 0.5, 1.5, -2.0, 1.0, 0.0] * 4
+    rows = []
+    rows.append([g * 2.0 ** -7 for g in grid])                      # amax 6 * 2^-7 -> scale -7
+    rows.append([7.0 * 2.0 ** 3] + [1.0 * 2.0 ** 3] * 31)           # amax 7 * 2^3: 7 saturates to 6
+    rows.append([4.0 * 2.0 ** -2] + [-0.5 * 2.0 ** -2] * 31)        # amax 4 * 2^k: exponent k
+    rows.append([3.9] + [0.25] * 31)                                 # floor(log2 3.9) = 1: shared -1
+    rows.append([0.0] * 32)                                          # zero block -> code 0, scale 0
+    rows.append([2.0 ** -130] + [0.0] * 31)                          # clamp at -127
+    w = np.array(rows, np.float32)
+    codes, scales = F.quantize_mx(w)
+    assert scales.reshape(-1).tolist() == [120, 130, 125, 126, 0, 0]
+    assert codes[0].tolist() == [F.e2m1_encode(g).item() for g in grid]
+    assert codes[1, 0] == 7 and codes[1, 1] == 2
+    assert codes[2, 0] == 6 and codes[2, 1] == 9
+    assert codes[3, 0] == 7 and codes[3, 1] == 1              # 3.9 * 2 -> 6 (saturated), 0.25 * 2 = 0.5
+    assert not codes[4].any()
+    # 2^-130 * 2^127 = 1/8: rounds to 0 (below 0.25)
+    assert codes[5, 0] == 0
+    rng = np.random.default_rng(3)
+    wr = (rng.standard_normal((6, 64)) * np.exp(rng.uniform(-12, 8, (6, 1)))).astype(np.float32)
+    c2, s2 = F.quantize_mx(wr)
+    for r in range(6):
+        for b in range(2):
+            sc, cc = _brute_mx_block(wr[r, 32 * b:32 * b + 32])
+            assert s2[r, b] == sc and c2[r, 32 * b:32 * b + 32].tolist() == cc
+
+
+def test_mx_record_layout_and_round_trip():
+    H, I = 4096, 2048
+    lay = F.record_layout(H, I, "mxfp4")
+    assert lay["gu_scales"][1] == 2 * I * H // 32 and lay["d_scales"][1] == H * I // 32
+    assert lay["raw_bytes"] == 3 * H * I // 2 + 3 * H * I // 32 + 8
+    assert lay["bytes"] % 256 == 0
+    rng = np.random.default_rng(4)
+    h, i = 64, 32
+    w_gu = (rng.standard_normal((2 * i, h)) * 0.02).astype(np.float32)
+    w_d = (rng.standard_normal((h, i)) * 0.02).astype(np.float32)
+    rec = F.encode_record(w_gu, w_d, "mxfp4")
+    f = F.record_fields(rec, h, i, "mxfp4")
+    assert f["s_gu"] == 1.0 and f["s_d"] == 1.0
+    g, d = F.decode_record(rec, h, i, "mxfp4")
+    c, s = F.quantize_mx(w_gu)
+    assert np.array_equal(g, F.e2m1_decode(c) * np.repeat(2.0 ** (s.astype(np.int64) - 127), 32, axis=1))
+    # every value of the decoded weights is on its block's E2M1 grid
+    assert np.all(np.abs(d) <= 6 * np.repeat(F.e8m0_decode(f["d_scales"]), 32, axis=1))
+
+
+def test_mx_and_nvfp4_records_of_the_same_values_decode_alike():
+    """Blocks whose scales are powers of two inside E4M3's range: the MXFP4 record
+    (E8M0 per 32) and an NVFP4 record with those scales (E4M3 per 16, tensor scale 1)
+    hold the same weights."""
+    rng = np.random.default_rng(5)
+    h, i = 64, 32
+    lay_n, lay_m = F.record_layout(h, i), F.record_layout(h, i, "mxfp4")
+    recs = {"nvfp4": np.zeros(lay_n["bytes"], np.uint8), "mxfp4": np.zeros(lay_m["bytes"], np.uint8)}
+    for name, rows, k in (("gu", 2 * i, h), ("d", h, i)):
+        codes = rng.integers(0, 16, (rows, k)).astype(np.uint8)
+        exps = rng.integers(-9, 9, (rows, k // 32))                 # E4M3 holds 2^-9 .. 2^8
+        e4m3 = {F.e4m3_decode(c).item(): c for c in range(0x7F)}
+        n_sc = np.repeat(np.vectorize(lambda e: e4m3[2.0 ** e])(exps), 2, axis=1).astype(np.uint8)
+        for fmt, sc in (("nvfp4", n_sc), ("mxfp4", (exps + 127).astype(np.uint8))):
+            lay = F.record_layout(h, i, fmt)
+            off, size = lay[name + "_codes"]
+            recs[fmt][off:off + size] = F.pack_nibbles(codes).reshape(-1)
+            off, size = lay[name + "_scales"]
+            recs[fmt][off:off + size] = sc.reshape(-1)
+    for fmt in recs:
+        lay = F.record_layout(h, i, fmt)
+        for t in ("s_gu", "s_d"):
+            off, size = lay[t]
+            recs[fmt][off:off + size] = np.float32([1.0]).view(np.uint8)
+    gn, dn = F.decode_record(recs["nvfp4"], h, i)
+    gm, dm = F.decode_record(recs["mxfp4"], h, i, "mxfp4")
+    assert np.array_equal(gn, gm) and np.array_equal(dn, dm)
