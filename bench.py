@@ -362,10 +362,11 @@ def roofline_ms(cnt, hbm_gbs, b_p):
 class DecodeRun:
     """A decode workload over one cache: reset + warm-up + timed graph replays."""
 
-    def __init__(self, ft, wlm, s, pool_ptr, shared, split, seed, steps):
+    def __init__(self, ft, wlm, s, pool_ptr, shared, split, seed, steps, fmt="nvfp4"):
         self.ft, self.s = ft, s
         self.cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool_ptr, shared=shared,
-                                    split=split, capacity_max=max([s.C] + list(s.resize.values())))
+                                    split=split, capacity_max=max([s.C] + list(s.resize.values())),
+                                    fmt=fmt)
         self.wl = wlm.DecodeWorkload(s, seed=seed, steps=steps)
         self.graph = wlm.StepGraph(self.wl, self.cache)
         self.steps = steps
@@ -496,6 +497,7 @@ def native(args, rank, world):
     pf = None
     if not args.no_prefill:
         pf = native_prefill(args, ft, wlm, pool, b_p, world)
+        pf["mxfp4"] = prefill_mx_leg(args, ft, wlm, world)
 
     # ---- headline: interleaved device-timed and e2e passes
     steps = args.warmup + args.steps
@@ -602,9 +604,9 @@ def native(args, rank, world):
 
 
 def decode_leg(ft, wlm, s, pool_ptr, shared, mode, f_q16, seed, warmup, steps, rec_bytes,
-               hbm_gbs, b_p, world, stream):
+               hbm_gbs, b_p, world, stream, fmt="nvfp4"):
     run = DecodeRun(ft, wlm, s, pool_ptr, shared, wlm.split_tuple(mode, f_q16), seed,
-                    warmup + steps)
+                    warmup + steps, fmt=fmt)
     ms = max_over_ranks(run.timed(warmup, world, stream), world)
     cnt = decode_counts(run.wl, warmup, warmup + steps, rec_bytes, s.shared)
     status = ft.ft_cache_status(run.cache.handle)
@@ -644,6 +646,18 @@ def dsv4_legs(args, ft, wlm, hbm_gbs, world, stream):
     legs["stress"] = leg
     for v in legs.values():
         v["b_p_gbs"] = b_p
+    pool.free()
+    # the same layers from natively MXFP4 records (E8M0 scale per 32)
+    rec_mx = ft.ft_record_bytes(s.H, s.I, "mxfp4")
+    pool = wlm.build_pool(args.seed, s.L, s.E, s.H, s.I, fmt="mxfp4")
+    b_p_mx, _ = measure_b_p(ft, pool, torch)
+    for B in (1, 4):
+        sb = replace(s, B=B)
+        leg = decode_leg(ft, wlm, sb, pool.ptr, None, "qstar", 32768, args.seed, 32, 256,
+                         rec_mx, hbm_gbs, b_p_mx, world, stream, fmt="mxfp4")
+        leg["b_p_gbs"] = b_p_mx
+        leg["record_format"] = "mxfp4"
+        legs[f"dsv4_mxfp4_B{B}_f1/2"] = leg
     pool.free()
     return legs
 
@@ -824,6 +838,48 @@ def prefill_on_demand_leg(args, ft, wlm, pool, b_p, world, xs, routes, y, capaci
             "gemm1_ms_per_layer": prof["prefill_gemm1"][0] / L, "gemm2_ms_per_layer": prof["prefill_gemm2"][0] / L,
             "note": "chunk from an emptied cache each time; DOUBLE_BUFFER asked for, 200 < 2E slots: "
                     "on-demand fallback; gathers and GEMMs of a group run one after the other"}
+
+
+def prefill_mx_leg(args, ft, wlm, world):
+    """The Qwen-shaped chunk from an MXFP4 pool (E8M0 scale per 32), double-buffered."""
+    import torch
+    import synth
+    s = wlm.SHAPES[args.prefill_workload]
+    T, L = s.T, s.L
+    rec = ft.ft_record_bytes(s.H, s.I, "mxfp4")
+    pool = wlm.build_pool(args.seed, L, s.E, s.H, s.I, fmt="mxfp4")
+    b_p, _ = measure_b_p(ft, pool, torch)
+    cache = ft.ExpertCache(L, s.E, s.H, s.I, s.k, 1, s.C, pool.ptr, T_max=T, fmt="mxfp4")
+    xs = [synth.prefill_x(args.seed, l, T, s.H, "cuda") for l in range(L)]
+    routes = [synth.prefill_routes(args.seed, l, T, s.E, s.k, "cuda") for l in range(L)]
+    y = torch.empty((T, s.H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def chunk():
+        for l in range(L):
+            ft.ft_moe_prefill_layer(cache.handle, l, xs[l], routes[l][0], routes[l][1], T, s.k, y,
+                                    ft.FT_PREFILL_DOUBLE_BUFFER)
+
+    chunk()
+    ms_all = []
+    for _ in range(2):
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        chunk()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_all.append(max_over_ranks(e0.elapsed_time(e1), world))
+    status = ft.ft_cache_status(cache.handle)
+    cache.close()
+    pool.free()
+    ms = statistics.median(ms_all)
+    link_ms = L * s.E * rec / (b_p * 1e9) * 1e3
+    return {"record_format": "mxfp4", "record_bytes": rec, "ms_per_chunk": ms,
+            "tok_s": T * world / (ms / 1e3), "repeats_ms": [round(v, 2) for v in ms_all],
+            "link_ms": link_ms, "frac": link_ms / ms, "b_p_gbs": b_p, "device_status": status}
 
 
 def prefill_only(args, world):

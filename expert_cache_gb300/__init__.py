@@ -17,7 +17,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libft.so")
 
 FT_OK, FT_ERR_ARG, FT_ERR_CUDA, FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, FT_ERR_UNPINNED = range(7)
-FT_DEV_BAD_ID, FT_DEV_TIMEOUT = 0x1, 0x2
+FT_DEV_BAD_ID, FT_DEV_TIMEOUT, FT_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
+FT_FORMAT_NVFP4, FT_FORMAT_MXFP4 = 0, 1
+FORMATS = {"nvfp4": FT_FORMAT_NVFP4, "mxfp4": FT_FORMAT_MXFP4}
 FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR = 0, 1
 FT_PREFILL_DOUBLE_BUFFER = 1
 FT_PREFILL_DEBUG_X = 2
@@ -44,7 +46,7 @@ class FtCacheDesc(ctypes.Structure):
                 ("k_max", c_int32), ("B_max", c_int32), ("capacity", c_int32),
                 ("capacity_max", c_int32), ("T_max", c_int32),
                 ("host_pool", c_void_p), ("slot_buf", c_void_p), ("workspace", c_void_p),
-                ("shared_experts", c_void_p), ("split", FtSplit)]
+                ("shared_experts", c_void_p), ("split", FtSplit), ("format", c_int32)]
 
 
 def _sig(name, res, *args):
@@ -57,6 +59,10 @@ def _sig(name, res, *args):
 _P = ctypes.POINTER
 _f = {
     "ft_record_bytes": _sig("ft_record_bytes", c_int32, c_int32, c_int32, _P(c_size_t)),
+    "ft_record_bytes_format": _sig("ft_record_bytes_format", c_int32, c_int32, c_int32, c_int32,
+                                   _P(c_size_t)),
+    "ft_quantize_experts_mx": _sig("ft_quantize_experts_mx", c_int32, c_void_p, c_void_p, c_int32,
+                                   c_int32, c_int32, c_void_p, c_void_p),
     "ft_cache_required_sizes": _sig("ft_cache_required_sizes", c_int32, _P(FtCacheDesc),
                                     _P(c_size_t), _P(c_size_t)),
     "ft_cache_create": _sig("ft_cache_create", c_int32, _P(FtCacheDesc), _P(c_void_p)),
@@ -131,9 +137,12 @@ def _check(status, handle=None):
 
 # ----------------------------------------------------------------- thin wrappers
 
-def ft_record_bytes(H, I):
+def ft_record_bytes(H, I, fmt="nvfp4"):
     out = c_size_t()
-    _check(_f["ft_record_bytes"](H, I, ctypes.byref(out)))
+    if fmt == "nvfp4":
+        _check(_f["ft_record_bytes"](H, I, ctypes.byref(out)))
+    else:
+        _check(_f["ft_record_bytes_format"](FORMATS[fmt], H, I, ctypes.byref(out)))
     return out.value
 
 
@@ -249,8 +258,9 @@ def ft_check_bounded_waits():
     return bits.value
 
 
-def ft_quantize_experts(w_gu, w_d, n, H, I, records, stream=None):
-    _check(_f["ft_quantize_experts"](_ptr(w_gu), _ptr(w_d), n, H, I, _ptr(records), _stream(stream)))
+def ft_quantize_experts(w_gu, w_d, n, H, I, records, stream=None, fmt="nvfp4"):
+    name = "ft_quantize_experts" if fmt == "nvfp4" else "ft_quantize_experts_mx"
+    _check(_f[name](_ptr(w_gu), _ptr(w_d), n, H, I, _ptr(records), _stream(stream)))
 
 
 def ft_pinned_alloc(nbytes):
@@ -318,11 +328,12 @@ class ExpertCache:
     and the ft_cache handle over a caller-provided pinned host pool."""
 
     def __init__(self, L, E, H, I, k_max, B_max, capacity, host_pool_ptr, shared=None,
-                 split=(FT_SPLIT_FULL_OFFLOAD, 65536), capacity_max=0, T_max=0, device="cuda"):
+                 split=(FT_SPLIT_FULL_OFFLOAD, 65536), capacity_max=0, T_max=0, device="cuda",
+                 fmt="nvfp4"):
         import torch
         self.L, self.E, self.H, self.I = L, E, H, I
         self.desc = FtCacheDesc(L, E, H, I, k_max, B_max, capacity, capacity_max, T_max,
-                                None, None, None, None, FtSplit(*split))
+                                None, None, None, None, FtSplit(*split), FORMATS[fmt])
         self.rec_bytes, ws_bytes = ft_cache_required_sizes(self.desc)
         cmax = capacity_max or capacity
         self.slot_buf = torch.empty(cmax * self.rec_bytes, dtype=torch.uint8, device=device)

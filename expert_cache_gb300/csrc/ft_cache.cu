@@ -105,6 +105,7 @@ static ft_status check_desc(const ft_cache_desc* d) {
     if ((long long)d->L * d->E > (1LL << 30) || d->T_max < 0) return FT_ERR_ARG;
     if (d->split.mode != FT_SPLIT_FULL_OFFLOAD && d->split.mode != FT_SPLIT_QSTAR) return FT_ERR_ARG;
     if (d->split.mode == FT_SPLIT_QSTAR && (d->split.f_q16 < 1 || d->split.f_q16 > 65536)) return FT_ERR_ARG;
+    if (d->format != FT_FORMAT_NVFP4 && d->format != FT_FORMAT_MXFP4) return FT_ERR_ARG;
     return FT_OK;
 }
 
@@ -133,6 +134,7 @@ DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids
     a.L = c->d.L; a.E = c->d.E; a.H = c->d.H; a.I = c->d.I; a.C = c->C;
     a.layer = layer; a.B = B; a.k = k;
     a.R_cap = c->d.B_max * c->d.k_max;
+    a.mx = c->d.format == FT_FORMAT_MXFP4 ? 1 : 0;
     a.split_mode = c->d.split.mode;
     a.f_q16 = c->d.split.f_q16;
     a.x = static_cast<const __nv_bfloat16*>(x);
@@ -172,11 +174,18 @@ ft_status ft_record_bytes(int32_t H, int32_t I, size_t* bytes) {
     return FT_OK;
 }
 
+ft_status ft_record_bytes_format(int32_t format, int32_t H, int32_t I, size_t* bytes) {
+    if (format != FT_FORMAT_NVFP4 && format != FT_FORMAT_MXFP4) return FT_ERR_ARG;
+    if (!bytes || H < 64 || H % 64 || I < 32 || I % 32) return FT_ERR_ARG;
+    *bytes = record_layout(H, I, format).bytes;
+    return FT_OK;
+}
+
 ft_status ft_cache_required_sizes(const ft_cache_desc* d, size_t* record_bytes,
                                   size_t* workspace_bytes) {
     ft_status s = check_desc(d);
     if (s != FT_OK) return s;
-    if (record_bytes) *record_bytes = record_layout(d->H, d->I).bytes;
+    if (record_bytes) *record_bytes = record_layout(d->H, d->I, d->format).bytes;
     if (workspace_bytes) *workspace_bytes = ws_layout(*d).total;
     return FT_OK;
 }
@@ -210,7 +219,7 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
     if (!c) return FT_ERR_ARG;
     c->d = *d;
     if (c->d.capacity_max <= 0) c->d.capacity_max = d->capacity;
-    c->rec = record_layout(d->H, d->I);
+    c->rec = record_layout(d->H, d->I, d->format);
     c->ws = ws_layout(c->d);
     c->C = d->capacity;
     c->host_pool_dev = static_cast<const uint8_t*>(pa.devicePointer);
@@ -519,6 +528,16 @@ ft_status ft_quantize_experts(const float* w_gu, const float* w_d, int32_t n, in
     if (!aligned(w_gu, 16) || !aligned(w_d, 16) || !aligned(records, 256)) return FT_ERR_ARG;
     cudaError_t e = launch_quantize(w_gu, w_d, n, H, I, static_cast<uint8_t*>(records),
                                     record_layout(H, I).bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_quantize_experts_mx(const float* w_gu, const float* w_d, int32_t n, int32_t H,
+                                 int32_t I, void* records, void* stream) {
+    if (!w_gu || !w_d || !records || n < 1 || H < 64 || H % 64 || I < 32 || I % 32) return FT_ERR_ARG;
+    if (!aligned(w_gu, 16) || !aligned(w_d, 16) || !aligned(records, 256)) return FT_ERR_ARG;
+    cudaError_t e = launch_quantize_mx(w_gu, w_d, n, H, I, static_cast<uint8_t*>(records),
+                                       record_layout(H, I, FT_FORMAT_MXFP4).bytes,
+                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FT_OK : FT_ERR_CUDA;
 }
 

@@ -239,6 +239,21 @@ __device__ __forceinline__ float dot8_f16(const uint32_t* c, uint4 x, float acc)
     return acc;
 }
 
+// E8M0 scale byte -> fp32 2^(c - 127) (c = 0: the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t c) {
+    return __uint_as_float(c ? c << 23 : 0x00400000u);
+}
+
+// Scales of the two 16-element halves of 32-element chunk ch of a staged scale row:
+// NVFP4 two E4M3 bytes, MXFP4 one E8M0 byte for both.
+__device__ __forceinline__ float2 chunk_scales(const uint8_t* srow_p, int ch, int mx) {
+    if (mx) {
+        const float s = e8m0_value(srow_p[ch]);
+        return make_float2(s, s);
+    }
+    return e4m3x2_to_float2(*reinterpret_cast<const unsigned short*>(srow_p + 2 * ch));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -591,9 +606,10 @@ __device__ __forceinline__ void stage_gate_up(const DecodeArgs& a, UnitRef ur, i
                                               uint8_t* ws, uint64_t* bar) {
     const int H = a.H, I = a.I, P = decode_pairs(H);
     const size_t cg = (size_t)(tile * P) * (H / 2), cu = (size_t)(I + tile * P) * (H / 2);
-    const size_t sg = a.off_gu_scales + (size_t)(tile * P) * (H / 16);
-    const size_t su = a.off_gu_scales + (size_t)(I + tile * P) * (H / 16);
-    const uint32_t nc = (uint32_t)P * (H / 2), ns = (uint32_t)P * (H / 16);
+    const int sb = a.mx ? 32 : 16;                                   // scale block
+    const size_t sg = a.off_gu_scales + (size_t)(tile * P) * (H / sb);
+    const size_t su = a.off_gu_scales + (size_t)(I + tile * P) * (H / sb);
+    const uint32_t nc = (uint32_t)P * (H / 2), ns = (uint32_t)P * (H / sb);
     uint8_t* d = ur.dst;
     if (d == nullptr) {
         arm_bulk(bar, 2 * (nc + ns));
@@ -617,7 +633,7 @@ __device__ void gate_up_rows(const DecodeArgs& a, const SmemStatic& S, const uin
                              const uint8_t* ws, int tile, int pair0, const int* xrow, float s_gu) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, P = decode_pairs(H);
-    const int nch = H / 32, pieces = H / 8, rb = H / 2, srow = H / 16;
+    const int nch = H / 32, pieces = H / 8, rb = H / 2, srow = H / (a.mx ? 32 : 16);
 #pragma unroll 1
     for (int p = warp; p < P; p += kWarps) {
         float ag[NT], au[NT];
@@ -631,8 +647,8 @@ __device__ void gate_up_rows(const DecodeArgs& a, const SmemStatic& S, const uin
         for (int ch = lane; ch < nch; ch += 32) {
             const uint4 wg = *reinterpret_cast<const uint4*>(cgp + ch * 16);
             const uint4 wu = *reinterpret_cast<const uint4*>(cup + ch * 16);
-            const float2 fg = e4m3x2_to_float2(*reinterpret_cast<const unsigned short*>(sgp + 2 * ch));
-            const float2 fu = e4m3x2_to_float2(*reinterpret_cast<const unsigned short*>(sup + 2 * ch));
+            const float2 fg = chunk_scales(sgp, ch, a.mx);
+            const float2 fu = chunk_scales(sup, ch, a.mx);
             const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
             const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
             float pg[2][NT], pu[2][NT];
@@ -732,8 +748,9 @@ __device__ __forceinline__ void stage_down(const DecodeArgs& a, UnitRef ur, int 
                                            uint8_t* ds, uint64_t* bar) {
     const int I = a.I, R = decode_rows(I);
     const size_t co = a.off_d_codes + (size_t)(rt * R) * (I / 2);
-    const size_t so = a.off_d_scales + (size_t)(rt * R) * (I / 16);
-    const uint32_t nc = (uint32_t)R * (I / 2), ns = (uint32_t)R * (I / 16);
+    const int sb = a.mx ? 32 : 16;
+    const size_t so = a.off_d_scales + (size_t)(rt * R) * (I / sb);
+    const uint32_t nc = (uint32_t)R * (I / 2), ns = (uint32_t)R * (I / sb);
     uint8_t* d = ur.dst;
     if (d == nullptr) {
         arm_bulk(bar, nc + ns);
@@ -761,7 +778,7 @@ __device__ void down_rows(const DecodeArgs& a, const SmemStatic& S, const float*
                           const uint8_t* ds, int rt, uint32_t tokmask, int g0, float s_d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, R = decode_rows(I);
-    const int nch = I / 32, rb = I / 2, srow = I / 16, hpieces = I / 4;
+    const int nch = I / 32, rb = I / 2, srow = I / (a.mx ? 32 : 16), hpieces = I / 4;
     int lpr = 1;
     while (lpr < nch && lpr < 32) lpr <<= 1;
     const int rpi = 32 / lpr, sub = lane / lpr, li = lane % lpr;
@@ -779,7 +796,7 @@ __device__ void down_rows(const DecodeArgs& a, const SmemStatic& S, const float*
 #pragma unroll 1
         for (int ch = li; rok && ch < nch; ch += lpr) {
             const uint4 w4 = *reinterpret_cast<const uint4*>(dc + (size_t)rl * rb + ch * 16);
-            const float2 f = e4m3x2_to_float2(*reinterpret_cast<const unsigned short*>(ds + rl * srow + 2 * ch));
+            const float2 f = chunk_scales(ds + rl * srow, ch, a.mx);
             const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
             for (int blk = 0; blk < 2; ++blk) {

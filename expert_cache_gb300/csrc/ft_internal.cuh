@@ -56,13 +56,17 @@ struct RecordLayout {
     size_t raw, bytes;
 };
 
-inline RecordLayout record_layout(int H, int I) {
+// Scale block length along K: 16 (NVFP4, E4M3 scales) or 32 (MXFP4, E8M0 scales).
+inline int scale_block(int format) { return format == FT_FORMAT_MXFP4 ? 32 : 16; }
+
+inline RecordLayout record_layout(int H, int I, int format = FT_FORMAT_NVFP4) {
     RecordLayout r;
+    const size_t sb = (size_t)scale_block(format);
     size_t off = 0;
     r.gu_codes = off;  off += (size_t)2 * I * H / 2;
-    r.gu_scales = off; off += (size_t)2 * I * H / 16;
+    r.gu_scales = off; off += (size_t)2 * I * H / sb;
     r.d_codes = off;   off += (size_t)H * I / 2;
-    r.d_scales = off;  off += (size_t)H * I / 16;
+    r.d_scales = off;  off += (size_t)H * I / sb;
     r.s_gu = off;      off += 4;
     r.s_d = off;       off += 4;
     r.raw = off;
@@ -117,6 +121,7 @@ struct DecodeArgs {
     size_t off_gu_scales, off_d_codes, off_d_scales, off_s_gu, off_s_d;
     int L, E, H, I, C, layer, B, k;
     int R_cap;             // B_max * k_max: sizes of the per-call arrays
+    int mx;                // 1: MXFP4 records (E8M0 scale per 32), 0: NVFP4 (E4M3 per 16)
     int split_mode;
     unsigned f_q16;
     const __nv_bfloat16* x;
@@ -141,6 +146,8 @@ cudaError_t check_bounded_waits(unsigned* expired);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s);
+cudaError_t launch_quantize_mx(const float* w_gu, const float* w_d, int n, int H, int I,
+                               uint8_t* records, size_t rec_bytes, cudaStream_t s);
 
 int sm_count();
 

@@ -172,6 +172,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     g.I = d.I; g.H = d.H;
     g.slot0 = b * d.E;
     g.slot_of = nullptr;
+    g.mx = d.format == FT_FORMAT_MXFP4 ? 1 : 0;
     g.slot_buf = c->slot_buf;
     g.rec_bytes = rec;
     g.offsets = a.offsets;

@@ -95,6 +95,82 @@ __global__ void block_quant_kernel(const float* w_gu, const float* w_d, int n_ex
     }
 }
 
+// MXFP4: one thread per 32-element block of every matrix (the microscaling
+// conversion rule; fp32 IEEE steps): shared = floor(log2(amax)) - 2 clamped to
+// [-127, 127] (amax 0: -127); code = E2M1_RNE_sat(v * 2^-shared).
+__global__ void block_quant_mx_kernel(const float* w_gu, const float* w_d, int n_exp, int H, int I,
+                                      uint8_t* records, size_t rec_bytes, RecordOffsets off) {
+    const size_t blocks_gu = (size_t)2 * I * H / 32, blocks_d = (size_t)H * I / 32;
+    const size_t per = blocks_gu + blocks_d;
+    const size_t total = per * n_exp;
+    for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+         g += (size_t)gridDim.x * blockDim.x) {
+        const size_t n = g / per, bi = g % per;
+        uint8_t* rec = records + n * rec_bytes;
+        const float* src;
+        uint8_t* codes;
+        uint8_t* scale;
+        if (bi < blocks_gu) {
+            src = w_gu + (size_t)n * 2 * I * H + bi * 32;
+            codes = rec + off.gu_codes + bi * 16;
+            scale = rec + off.gu_scales + bi;
+        } else {
+            const size_t b = bi - blocks_gu;
+            src = w_d + (size_t)n * H * I + b * 32;
+            codes = rec + off.d_codes + b * 16;
+            scale = rec + off.d_scales + b;
+        }
+        float v[32];
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = s4[j];
+            v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        int shared = -127;
+        if (amax > 0.f) {
+            const uint32_t b = __float_as_uint(amax);
+            const int ef = (int)(b >> 23);
+            // floor(log2(amax)): the exponent of a normal number, or the position of the
+            // leading mantissa bit of a subnormal one
+            const int fl = ef ? ef - 127 : (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+            shared = max(-127, min(127, fl - 2));
+        }
+        const int mexp = 127 - shared;                     // 2^-shared as fp32 bits
+        const float mul = __uint_as_float(mexp ? (uint32_t)mexp << 23 : 0x00400000u);
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            w[j >> 3] |= (uint32_t)e2m1_encode_rne(__fmul_rn(v[j], mul)) << (4 * (j & 7));
+        *reinterpret_cast<uint4*>(codes) = make_uint4(w[0], w[1], w[2], w[3]);
+        *scale = (uint8_t)(shared + 127);
+    }
+}
+
+__global__ void unit_tensor_scales_kernel(uint8_t* records, size_t rec_bytes, size_t off_s_gu, size_t off_s_d,
+                                          int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        *reinterpret_cast<float*>(records + (size_t)i * rec_bytes + off_s_gu) = 1.0f;
+        *reinterpret_cast<float*>(records + (size_t)i * rec_bytes + off_s_d) = 1.0f;
+    }
+}
+
+cudaError_t launch_quantize_mx(const float* w_gu, const float* w_d, int n, int H, int I,
+                               uint8_t* records, size_t rec_bytes, cudaStream_t s) {
+    const RecordLayout r = record_layout(H, I, FT_FORMAT_MXFP4);
+    RecordOffsets off{r.gu_codes, r.gu_scales, r.d_codes, r.d_scales, r.s_gu, r.s_d};
+    cudaMemsetAsync(records, 0, (size_t)n * rec_bytes, s);
+    unit_tensor_scales_kernel<<<(n + 255) / 256, 256, 0, s>>>(records, rec_bytes, r.s_gu, r.s_d, n);
+    const size_t total = ((size_t)2 * I * H / 32 + (size_t)H * I / 32) * n;
+    size_t grid = (total + 255) / 256;
+    if (grid > (size_t)sm_count() * 16) grid = (size_t)sm_count() * 16;
+    block_quant_mx_kernel<<<(unsigned)grid, 256, 0, s>>>(w_gu, w_d, n, H, I, records, rec_bytes, off);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s) {
     const RecordLayout r = record_layout(H, I);

@@ -117,6 +117,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// An E8M0 scale (2^(c - 127)) as the UE4M3 byte of the same value: exact for
+// 2^-9 .. 2^8 (subnormal codes 1, 2, 4 below 2^-6); outside, the nearest end of that
+// range and *bad set.
+__device__ __forceinline__ uint32_t e8m0_to_ue4m3(uint32_t c, int* bad) {
+    const int k = (int)c - 127;
+    if (k >= -6 && k <= 8) return (uint32_t)(k + 7) << 3;
+    if (k >= -9 && k < -6) return 1u << (k + 9);
+    *bad = 1;
+    return k > 8 ? 0x78u : 0x01u;
+}
+
 struct TileInfo {
     int e, m0, rows, nt;
 };
@@ -175,6 +186,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ------------------------------------------------------------ producer
         int it = 0;
         bool ok = true;
+        int scale_bad = 0;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             const TileInfo ti = tile_info(g, tile);
             const int slot = g.slot_of ? g.slot_of[ti.e] : g.slot0 + ti.e;
@@ -210,9 +222,23 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int n = lane; n < kBN; n += 32) {
                     const int brow = g.kind == 1 ? (n < 128 ? ti.nt * 128 + n : g.I + ti.nt * 128 + (n - 128))
                                                  : ti.nt * kBN + n;
-                    const uint4 v = *reinterpret_cast<const uint4*>(rec + g.off_b_scales +
-                                                                    (size_t)brow * srow + ks * 16);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t w4[4];
+                    if (!g.mx) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(rec + g.off_b_scales +
+                                                                        (size_t)brow * srow + ks * 16);
+                        w4[0] = v.x; w4[1] = v.y; w4[2] = v.z; w4[3] = v.w;
+                    } else {
+                        // 8 E8M0 scales of 32 elements -> 16 UE4M3 scales of 16 (each twice)
+                        const uint2 v = *reinterpret_cast<const uint2*>(rec + g.off_b_scales +
+                                                                        (size_t)brow * (g.K / 32) + ks * 8);
+#pragma unroll
+                        for (int kb = 0; kb < 4; ++kb) {
+                            const uint32_t word = kb < 2 ? v.x : v.y;
+                            const uint32_t s0 = e8m0_to_ue4m3((word >> (16 * (kb & 1))) & 0xFF, &scale_bad);
+                            const uint32_t s1 = e8m0_to_ue4m3((word >> (16 * (kb & 1) + 8)) & 0xFF, &scale_bad);
+                            w4[kb] = s0 | (s0 << 8) | (s1 << 16) | (s1 << 24);
+                        }
+                    }
                     const int half = n >> 7, r = n & 127;
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb)
@@ -222,6 +248,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 mbar_arrive(&full_bar[s]);
             }
         }
+        if (scale_bad) atomicOr(g.status, FT_DEV_SCALE_RANGE);
         if (!ok) {
             // drain: wait (bounded) for this CTA's TMA copies still in flight
             for (int j = 1; j <= kStages && it - j >= 0; ++j) {

@@ -16,6 +16,7 @@ struct UmmaArgs {
     const uint8_t* slot_buf;
     size_t rec_bytes;
     size_t off_b_scales;        // record offset of the B scales (W_gu or W_d)
+    int mx;                     // 1: B scales are E8M0 per 32 (MXFP4 records)
     size_t off_tscale;          // record offset of the B tensor scale
     const uint8_t* a_scales;    // [R_max, K/16]
     const int32_t* offsets;     // [E + 1]

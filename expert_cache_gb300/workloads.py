@@ -17,9 +17,9 @@ from . import (FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR, ExpertCache, PinnedBuffer,
 
 
 def build_pool(seed: int, L: int, E: int, H: int, I: int, chunk_bytes: int = 1 << 30,
-               device: str = "cuda") -> PinnedBuffer:
-    """Pinned host pool of L*E NVFP4 records, flat id l*E + e."""
-    rec = ft_record_bytes(H, I)
+               device: str = "cuda", fmt: str = "nvfp4") -> PinnedBuffer:
+    """Pinned host pool of L*E records (NVFP4 or MXFP4), flat id l*E + e."""
+    rec = ft_record_bytes(H, I, fmt)
     n_all = L * E
     pool = PinnedBuffer(n_all * rec)
     host = pool.tensor()
@@ -33,19 +33,21 @@ def build_pool(seed: int, L: int, E: int, H: int, I: int, chunk_bytes: int = 1 <
         w_gu.copy_(a)
         w_d.copy_(b)
         del a, b
-        ft_quantize_experts(w_gu, w_d, n, H, I, stage)
+        ft_quantize_experts(w_gu, w_d, n, H, I, stage, fmt=fmt)
         host[f0 * rec:(f0 + n) * rec].copy_(stage[:n * rec])
     torch.cuda.synchronize()
     return pool
 
 
-def build_shared(seed: int, L: int, H: int, I: int, device: str = "cuda") -> torch.Tensor:
+def build_shared(seed: int, L: int, H: int, I: int, device: str = "cuda",
+                 fmt: str = "nvfp4") -> torch.Tensor:
     """Device records of the always-resident shared expert of each layer."""
-    rec = ft_record_bytes(H, I)
+    rec = ft_record_bytes(H, I, fmt)
     out = torch.empty(L * rec, dtype=torch.uint8, device=device)
     for l in range(L):
         a, b = synth.shared_weights(seed, l, H, I, device)
-        ft_quantize_experts(a.contiguous(), b.contiguous(), 1, H, I, out[l * rec:(l + 1) * rec])
+        ft_quantize_experts(a.contiguous(), b.contiguous(), 1, H, I, out[l * rec:(l + 1) * rec],
+                            fmt=fmt)
     torch.cuda.synchronize()
     return out
 

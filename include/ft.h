@@ -55,6 +55,17 @@ typedef int32_t ft_status;
 /* Bits of the device status word (ft_cache_status). */
 #define FT_DEV_BAD_ID    0x1 /* a route id outside [0, E) was masked */
 #define FT_DEV_TIMEOUT   0x2 /* a bounded device wait ran out */
+#define FT_DEV_SCALE_RANGE 0x4 /* prefill of MXFP4 experts: a block scale outside
+                                  2^-9..2^8 has no exact UE4M3 twin (clamped) */
+
+/* Expert record formats ([EXPLAINER §9.2]: NVFP4 on the NVFP4 machines; DeepSeek-V4-
+ * Flash's routed experts are natively MXFP4 and are consumed bit-exactly).
+ * FT_FORMAT_NVFP4: E2M1 codes, unsigned E4M3 scale per 16 elements, fp32 tensor scale
+ *   per matrix (the record layout above).
+ * FT_FORMAT_MXFP4: E2M1 codes, E8M0 scale per 32 elements (value 2^(c-127)); same
+ *   layout with the scale arrays [rows, K/32]; the two tensor-scale words are 1.0. */
+#define FT_FORMAT_NVFP4 0
+#define FT_FORMAT_MXFP4 1
 
 typedef struct ft_cache ft_cache;
 
@@ -86,10 +97,14 @@ typedef struct {
     const void* shared_experts; /* device, L records (always-resident shared expert,
                                weight 1, [JUHE "先纠正一个容易混淆的模型"]), or NULL */
     ft_split split;
+    int32_t format;         /* FT_FORMAT_NVFP4 (0) or FT_FORMAT_MXFP4 of host_pool and
+                               shared_experts */
 } ft_cache_desc;
 
-/* Bytes of one expert record (padded), for hidden H and intermediate I. */
+/* Bytes of one expert record (padded), for hidden H and intermediate I (NVFP4, and
+ * for a given format). */
 ft_status ft_record_bytes(int32_t H, int32_t I, size_t* bytes);
+ft_status ft_record_bytes_format(int32_t format, int32_t H, int32_t I, size_t* bytes);
 
 /* Record bytes and device workspace bytes needed by a descriptor (host pointers in
  * it are ignored).  The workspace holds the slot tables ([JUHE "生成阶段"]:
@@ -270,6 +285,12 @@ ft_status ft_check_bounded_waits(uint32_t* expired);
  *   records device uint8 [n, ft_record_bytes(H, I)]. */
 ft_status ft_quantize_experts(const float* w_gu, const float* w_d, int32_t n, int32_t H,
                               int32_t I, void* records, void* stream);
+/* The same for MXFP4 records (the conversion rule of the microscaling format, fp32 IEEE
+ * steps): shared = floor(log2(amax32)) - 2 clamped to [-127, 127] (amax 0: -127);
+ * scale code = shared + 127; code = E2M1_RNE_sat(w * 2^-shared); tensor scales 1.0.
+ * records device uint8 [n, ft_record_bytes_format(FT_FORMAT_MXFP4, H, I)]. */
+ft_status ft_quantize_experts_mx(const float* w_gu, const float* w_d, int32_t n, int32_t H,
+                                 int32_t I, void* records, void* stream);
 
 /* Page-locked, device-mapped host memory for the pool ([EXPLAINER §7.3]: pin the
  * pool; the caller fills it). */

@@ -9,17 +9,19 @@ REL_L2 = 5e-3          # ||y - y_ref|| / ||y_ref||
 MAX_ABS_RMS = 2e-2     # max |y - y_ref| / rms(y_ref)
 
 
-def oracle_experts(seed, H, I):
-    """Oracle RecordSource: weights regenerated on the CPU, quantised by the oracle."""
+def oracle_experts(seed, H, I, fmt="nvfp4", scale=1.0):
+    """Oracle RecordSource: weights regenerated on the CPU (times `scale`), quantised by
+    the oracle in format fmt."""
     return RecordSource(
-        lambda f: encode_record(*[w.numpy() for w in synth.expert_weights(seed, f, H, I, "cpu")]),
-        H, I)
+        lambda f: encode_record(*[w.numpy() * np.float32(scale)
+                                  for w in synth.expert_weights(seed, f, H, I, "cpu")], fmt),
+        H, I, fmt)
 
 
-def oracle_shared(seed, layer, H, I):
+def oracle_shared(seed, layer, H, I, fmt="nvfp4"):
     from oracle.formats import decode_record
-    rec = encode_record(*[w.numpy() for w in synth.shared_weights(seed, layer, H, I, "cpu")])
-    return decode_record(rec, H, I)
+    rec = encode_record(*[w.numpy() for w in synth.shared_weights(seed, layer, H, I, "cpu")], fmt)
+    return decode_record(rec, H, I, fmt)
 
 
 def assert_close(y, y_ref, what=""):
