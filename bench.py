@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-legs", action="store_true")
-    ap.add_argument("--prefill-pairs", type=int, default=3)
+    ap.add_argument("--prefill-pairs", type=int, default=5)
     ap.add_argument("--prefill-workload", default="qwen_prefill")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill workload (its own pool; for profiling captures)")

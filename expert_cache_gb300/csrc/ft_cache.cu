@@ -380,6 +380,7 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
                         const float* topk_w, int32_t B, int32_t k, float* y,
                         int32_t* deferred, int32_t* route_slot, int32_t* counters,
                         void* stream) {
+    NvtxRange range("ft_moe_decode");
     if (!c) return FT_ERR_ARG;
     if (layer < 0 || layer >= c->d.L) return fail(c, FT_ERR_ARG, "layer out of range");
     if (B < 1 || B > c->d.B_max) return fail(c, FT_ERR_ARG, "B outside [1, B_max]");
@@ -412,6 +413,7 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
 // ------------------------------------------------------------------ resize / state
 
 ft_status ft_cache_resize(ft_cache* c, int32_t new_capacity, void* new_slot_buf, void* stream) {
+    NvtxRange range("ft_cache_resize");
     if (!c) return FT_ERR_ARG;
     if (new_capacity < 1 || new_capacity > c->d.capacity_max)
         return fail(c, FT_ERR_ARG, "new_capacity outside [1, capacity_max]");
@@ -457,6 +459,7 @@ ft_status ft_cache_snapshot(ft_cache* c, int32_t* slot_for_id, int32_t* id_of_sl
 
 ft_status ft_cache_restore(ft_cache* c, const int32_t* slot_for_id, const int32_t* id_of_slot,
                            const int64_t* usage, int64_t tick, void* stream) {
+    NvtxRange range("ft_cache_restore");
     if (!c) return FT_ERR_ARG;
     if (!slot_for_id || !id_of_slot || !usage || tick < 0) return fail(c, FT_ERR_ARG, "NULL table or tick < 0");
     const int C = c->C;

@@ -61,6 +61,7 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
                                           const int32_t* topk_ids, const float* topk_w,
                                           int32_t B, int32_t k, float* y, int32_t* deferred,
                                           int32_t* route_slot, int32_t* counters, void* stream) {
+    NvtxRange range("ft_moe_decode_static");
     if (!c) return FT_ERR_ARG;
     auto fail = [&](ft_status s, const char* m) { snprintf(c->err, sizeof(c->err), "%s", m); return s; };
     if (layer < 0 || layer >= c->d.L) return fail(FT_ERR_ARG, "layer out of range");

@@ -9,6 +9,8 @@
 #include <stddef.h>
 #include <utility>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/ft.h"
 
 namespace ft {
@@ -150,6 +152,15 @@ cudaError_t launch_quantize_mx(const float* w_gu, const float* w_d, int n, int H
                                uint8_t* records, size_t rec_bytes, cudaStream_t s);
 
 int sm_count();
+
+// NVTX range around a host API call: named spans on a profiler's timeline (host side;
+// nothing happens when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ----------------------------------------------------------------- device helpers
 #ifdef __CUDACC__

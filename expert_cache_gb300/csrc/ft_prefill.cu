@@ -35,6 +35,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
                                           const int32_t* topk_ids, const float* topk_w,
                                           int32_t T, int32_t k, float* y, int32_t flags,
                                           void* debug_h, void* stream) {
+    NvtxRange range("ft_moe_prefill_layer");
     if (!c) return FT_ERR_ARG;
     auto fail = [&](ft_status s, const char* m) { snprintf(c->err, sizeof(c->err), "%s", m); return s; };
     const ft_cache_desc& d = c->d;
