@@ -22,10 +22,11 @@
 //     pairs.  Up to 32 routes one warp decides with warp intrinsics while the
 //     other warps stage x; larger batches use the whole CTA.
 //  2. Gate/up items (unit, P row pairs; P * H/2 <= 16 KB per matrix) go to CTAs
-//     0, 1, ... in order.  The item's rows are staged in shared memory first: bulk
-//     copies (one thread) for hits and the shared expert; for fills every thread
-//     reads the rows from the pinned pool over the host link and writes them into
-//     the victim slot on the way (one link read per byte).  Warp w then computes
+//     0, 1, ... in order.  The item's rows are staged in shared memory first by bulk
+//     copies issued by one thread: from HBM for hits and the shared expert, from the
+//     device-mapped pinned pool over the host link for fills (one link read per
+//     byte, one request per run); a fill's rows are then bulk-stored from shared
+//     memory into its victim slot, which makes the fill resident.  Warp w then computes
 //     pairs w, w + 8, ... in rolled loops (the per-item code stays small enough
 //     for the instruction cache).  Meanwhile warps 1..7 of compute CTA z zero y's
 //     R-row tile z (mod the compute CTAs) and raise the tile's flag (release).
@@ -91,16 +92,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-__device__ __forceinline__ uint4 ldg16_stream(const void* p, uint64_t pol) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
-    return v;
-}
-__device__ __forceinline__ void stg16_stream(void* p, uint4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
-                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol) : "memory");
 }
 __device__ __forceinline__ uint4 ldg16_l1(const void* p) {        // read-only, kept in L1
     uint4 v;
@@ -539,58 +530,28 @@ struct UnitRef {
     uint8_t* dst;         // victim slot written on the way (fill), else nullptr
 };
 
-// Stage one block of n bytes (a multiple of 16, 16-byte aligned) into shared memory.
-// Hits and the shared expert: thread 0 issues a bulk copy completing on `bar` (armed
-// by the caller; the caller waits).  Fills: every thread loads 16-byte pieces from
-// the pinned pool, writes them to shared memory and into the slot (dst) on the way;
-// the pieces are in shared memory after the caller's next barrier.
-__device__ __forceinline__ void stage_block(const uint8_t* src, uint8_t* dst, uint8_t* sm, uint32_t n,
-                                            uint64_t* bar) {
-    if (dst == nullptr) {
-        if (threadIdx.x == 0) bulk_g2s(sm, src, n, bar);
-        return;
-    }
-    const int n16 = (int)(n / 16);
-    const uint64_t pol = evict_first_policy();
-    for (int q0 = threadIdx.x; q0 < n16; q0 += 4 * kThreads) {
-        uint4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = q0 + i * kThreads;
-            if (q < n16) v[i] = ldg16_stream(src + (size_t)q * 16, pol);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = q0 + i * kThreads;
-            if (q < n16) {
-                *reinterpret_cast<uint4*>(sm + (size_t)q * 16) = v[i];
-                stg16_stream(dst + (size_t)q * 16, v[i], pol);
-            }
-        }
-    }
+// Every item is staged the same way: thread 0 issues bulk copies (`cp.async.bulk`,
+// the tensor memory accelerator) of the item's runs into shared memory, completing on
+// an mbarrier the item's threads wait on.  For hits and the shared expert the source
+// is HBM; for fills it is the device-mapped pinned pool, read over the host link in
+// one request per run (no per-thread round trips), and once the bytes have landed
+// thread 0 bulk-stores them from shared memory into the victim slot (the write-through
+// that makes the fill resident).  Before a CTA restages a buffer it waits until its
+// earlier bulk stores have read it; before the CTA exits, until they are complete.
+
+// Bulk store of n bytes (a multiple of 16, both ends 16-byte aligned), shared -> global,
+// in the calling thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(smem_u32(src)), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// A fill item's share of the record: up to four runs, each (source in the pinned
-// pool, destination in the victim slot, destination in shared memory, 16-byte pieces).
-struct FillRuns {
-    const uint8_t* src[4];
-    uint8_t* dst[4];
-    uint8_t* sm[4];
-    int n16[4];                 // 0: run unused
-};
-
-// Stages a fill item through registers, run after run (each run coalesced and
-// contiguous; several runs in flight at once read the host link less efficiently
-// once two or more fills share it).  Each piece goes to shared memory and into the
-// victim slot on the way; the pieces are in shared memory after the caller's next
-// barrier.  Out of line, so that its registers do not add to the kernel's hot loops.
-__device__ __noinline__ void stage_fill(const FillRuns& fr) {
-#pragma unroll 1
-    for (int r = 0; r < 4; ++r)
-        if (fr.n16[r] > 0) stage_block(fr.src[r], fr.dst[r], fr.sm[r], (uint32_t)fr.n16[r] * 16, nullptr);
-}
-
-// Arms `bar` for `bytes` of bulk copies (thread 0; hits and the shared expert only).
+// Arms `bar` for `bytes` of bulk copies (thread 0).
 __device__ __forceinline__ void arm_bulk(uint64_t* bar, uint32_t bytes) {
     if (threadIdx.x == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -600,30 +561,49 @@ __device__ __forceinline__ void arm_bulk(uint64_t* bar, uint32_t bytes) {
 
 // ------------------------------------------------------------------ gate / up item
 
-// Weights of gate/up item `tile`: rows P*tile .. +P-1 of gate and of up, codes and
-// scales, into wc / ws (gate rows first).
+// Where gate/up item `tile` lives in a record: rows P*tile .. +P-1 of gate and of up,
+// codes and scales.
+struct GuRuns {
+    size_t cg, cu, sg, su;      // record offsets: gate codes, up codes, gate scales, up scales
+    uint32_t nc, ns;            // bytes of one matrix's codes / scales in the item
+};
+__device__ __forceinline__ GuRuns gu_runs(const DecodeArgs& a, int tile) {
+    const int H = a.H, I = a.I, P = decode_pairs(H), sb = a.mx ? 32 : 16;
+    GuRuns r;
+    r.cg = (size_t)(tile * P) * (H / 2);
+    r.cu = (size_t)(I + tile * P) * (H / 2);
+    r.sg = a.off_gu_scales + (size_t)(tile * P) * (H / sb);
+    r.su = a.off_gu_scales + (size_t)(I + tile * P) * (H / sb);
+    r.nc = (uint32_t)P * (H / 2);
+    r.ns = (uint32_t)P * (H / sb);
+    return r;
+}
+
+// Weights of gate/up item `tile` into wc / ws (gate rows first), bulk copies on `bar`.
 __device__ __forceinline__ void stage_gate_up(const DecodeArgs& a, UnitRef ur, int tile, uint8_t* wc,
                                               uint8_t* ws, uint64_t* bar) {
-    const int H = a.H, I = a.I, P = decode_pairs(H);
-    const size_t cg = (size_t)(tile * P) * (H / 2), cu = (size_t)(I + tile * P) * (H / 2);
-    const int sb = a.mx ? 32 : 16;                                   // scale block
-    const size_t sg = a.off_gu_scales + (size_t)(tile * P) * (H / sb);
-    const size_t su = a.off_gu_scales + (size_t)(I + tile * P) * (H / sb);
-    const uint32_t nc = (uint32_t)P * (H / 2), ns = (uint32_t)P * (H / sb);
-    uint8_t* d = ur.dst;
-    if (d == nullptr) {
-        arm_bulk(bar, 2 * (nc + ns));
-        stage_block(ur.src + cg, nullptr, wc, nc, bar);
-        stage_block(ur.src + cu, nullptr, wc + nc, nc, bar);
-        stage_block(ur.src + sg, nullptr, ws, ns, bar);
-        stage_block(ur.src + su, nullptr, ws + ns, ns, bar);
-        return;
+    const GuRuns r = gu_runs(a, tile);
+    if (threadIdx.x == 0) {
+        bulk_wait_read();                              // wc / ws no longer read by stores
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_tx(bar, 2 * (r.nc + r.ns));
+        bulk_g2s(wc, ur.src + r.cg, r.nc, bar);
+        bulk_g2s(wc + r.nc, ur.src + r.cu, r.nc, bar);
+        bulk_g2s(ws, ur.src + r.sg, r.ns, bar);
+        bulk_g2s(ws + r.ns, ur.src + r.su, r.ns, bar);
     }
-    const FillRuns fr{{ur.src + cg, ur.src + cu, ur.src + sg, ur.src + su},
-                      {d + cg, d + cu, d + sg, d + su},
-                      {wc, wc + nc, ws, ws + ns},
-                      {(int)nc / 16, (int)nc / 16, (int)ns / 16, (int)ns / 16}};
-    stage_fill(fr);
+}
+
+// A fill's staged gate/up item into its victim slot (thread 0, after the item landed).
+__device__ __forceinline__ void store_gate_up(const DecodeArgs& a, UnitRef ur, int tile, const uint8_t* wc,
+                                              const uint8_t* ws) {
+    const GuRuns r = gu_runs(a, tile);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bulk_s2g(ur.dst + r.cg, wc, r.nc);
+    bulk_s2g(ur.dst + r.cu, wc + r.nc, r.nc);
+    bulk_s2g(ur.dst + r.sg, ws, r.ns);
+    bulk_s2g(ur.dst + r.su, ws + r.ns, r.ns);
+    bulk_commit();
 }
 
 // h = silu(g) * u of the item's row pairs for NT tokens (x rows xrow[]), from the
@@ -696,10 +676,10 @@ __device__ void gate_up_item(const DecodeArgs& a, SmemStatic& S, uint4* xs, uint
                              bool staged_all) {
     const bool fill = ur.dst != nullptr;
     const float s_gu = *reinterpret_cast<const float*>(ur.src + a.off_s_gu);
-    if (!fill) {
-        if (!mbar_wait(&S.bar_w, par_w)) S.timeout = 1;
-        par_w ^= 1u;
-    }
+    const bool landed = mbar_wait(&S.bar_w, par_w);
+    if (!landed) S.timeout = 1;
+    par_w ^= 1u;
+    if (fill && landed && threadIdx.x == 0) store_gate_up(a, ur, tile, wc, ws);
     const int ntok = __popc(tokmask);
     for (int g0 = 0; g0 < ntok; g0 += kTok) {
         int toks[kTok];
@@ -743,29 +723,46 @@ __device__ __forceinline__ UnitRef unit_ref_of(const DecodeArgs& a, const Decisi
 
 // ------------------------------------------------------------------ down item
 
-// Weights of down item `rt`: rows R*rt .. +R-1 of W_d, codes and scales, into dc / ds.
+// Where down item `rt` lives in a record: rows R*rt .. +R-1 of W_d, codes and scales.
+struct DownRuns {
+    size_t co, so;
+    uint32_t nc, ns;
+};
+__device__ __forceinline__ DownRuns down_runs(const DecodeArgs& a, int rt) {
+    const int I = a.I, R = decode_rows(I), sb = a.mx ? 32 : 16;
+    DownRuns r;
+    r.co = a.off_d_codes + (size_t)(rt * R) * (I / 2);
+    r.so = a.off_d_scales + (size_t)(rt * R) * (I / sb);
+    r.nc = (uint32_t)R * (I / 2);
+    r.ns = (uint32_t)R * (I / sb);
+    return r;
+}
+
+// Weights of down item `rt` into dc / ds, bulk copies on `bar`.  A fill's item 0 also
+// copies the record's two tensor-scale words into the victim slot.
 __device__ __forceinline__ void stage_down(const DecodeArgs& a, UnitRef ur, int rt, uint8_t* dc,
                                            uint8_t* ds, uint64_t* bar) {
-    const int I = a.I, R = decode_rows(I);
-    const size_t co = a.off_d_codes + (size_t)(rt * R) * (I / 2);
-    const int sb = a.mx ? 32 : 16;
-    const size_t so = a.off_d_scales + (size_t)(rt * R) * (I / sb);
-    const uint32_t nc = (uint32_t)R * (I / 2), ns = (uint32_t)R * (I / sb);
-    uint8_t* d = ur.dst;
-    if (d == nullptr) {
-        arm_bulk(bar, nc + ns);
-        stage_block(ur.src + co, nullptr, dc, nc, bar);
-        stage_block(ur.src + so, nullptr, ds, ns, bar);
-        return;
+    const DownRuns r = down_runs(a, rt);
+    if (threadIdx.x == 0) {
+        bulk_wait_read();                              // dc / ds no longer read by stores
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_tx(bar, r.nc + r.ns);
+        bulk_g2s(dc, ur.src + r.co, r.nc, bar);
+        bulk_g2s(ds, ur.src + r.so, r.ns, bar);
     }
-    const FillRuns fr{{ur.src + co, ur.src + so, nullptr, nullptr},
-                      {d + co, d + so, nullptr, nullptr},
-                      {dc, ds, nullptr, nullptr},
-                      {(int)nc / 16, (int)ns / 16, 0, 0}};
-    stage_fill(fr);
-    if (rt == 0 && threadIdx.x < 2)     // tensor scales s_gu, s_d of the fill
-        reinterpret_cast<float*>(d + a.off_s_gu)[threadIdx.x] =
+    if (ur.dst != nullptr && rt == 0 && threadIdx.x < 2)   // tensor scales s_gu, s_d
+        reinterpret_cast<float*>(ur.dst + a.off_s_gu)[threadIdx.x] =
             reinterpret_cast<const float*>(ur.src + a.off_s_gu)[threadIdx.x];
+}
+
+// A fill's staged down item into its victim slot (thread 0, after the item landed).
+__device__ __forceinline__ void store_down(const DecodeArgs& a, UnitRef ur, int rt, const uint8_t* dc,
+                                           const uint8_t* ds) {
+    const DownRuns r = down_runs(a, rt);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bulk_s2g(ur.dst + r.co, dc, r.nc);
+    bulk_s2g(ur.dst + r.so, ds, r.ns);
+    bulk_commit();
 }
 
 // o = s_d * W_d h for the item's rows and NT tokens (the set bits g0 .. g0+NT-1 of
@@ -871,10 +868,10 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, const Decision& D,
         }
     }
     __syncthreads();
-    if (!fill) {
-        if (!mbar_wait(&S.bar_d, par_d)) timeout = 1;
-        par_d ^= 1u;
-    }
+    const bool landed = mbar_wait(&S.bar_d, par_d);
+    if (!landed) timeout = 1;
+    par_d ^= 1u;
+    if (fill && landed && threadIdx.x == 0) store_down(a, ur, rt, dc, ds);
     const int ntok = __popc(tokmask);
     for (int g0 = 0; g0 < ntok; g0 += kTok) {
         const int ntg = min(kTok, ntok - g0);
@@ -1387,6 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         down_item(a, S, D, hs, dc, ds, par_d, prefetch && p == p_first, unit_ref_of(a, D, q, n_routed, u), u,
                   u >= n_routed, rt, D.u_pair0[u], D.u_mask[u]);
     }
+    if (tid == 0) bulk_wait_all();                 // the fills' slot writes are complete
     if (tid == 0 && S.timeout) atomicOr(&a.sc->status, FT_DEV_TIMEOUT);
 }
 

@@ -318,10 +318,16 @@ __global__ void __launch_bounds__(1024, 1) pf_scan_kernel(PrefillArgs a) {
         const int e = threadIdx.x * ne + j;
         if (j < ne && e < E) {
             int run = 0;
-            for (int c = 0; c < n_chunks; ++c) {
-                const int v = a.chunk_cnt[(size_t)c * E + e];
-                a.chunk_cnt[(size_t)c * E + e] = run;
-                run += v;
+            for (int c0 = 0; c0 < n_chunks; c0 += 16) {   // 16 loads in flight, then the prefixes
+                int v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = c0 + i < n_chunks ? a.chunk_cnt[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (c0 + i < n_chunks) a.chunk_cnt[(size_t)(c0 + i) * E + e] = run;
+                    run += v[i];
+                }
             }
             tot[j] = run;
             tiles[j] = (run + 127) / 128;
