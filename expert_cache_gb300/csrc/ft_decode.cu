@@ -1371,6 +1371,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         if (tid == 0) st_relaxed_u64(a.hflag + (size_t)u * T1 + tile, tagged(0.f, S.tag));
     }
     if (prefetch_due) prefetch_down(a, D, q, n_routed, p_first / T2, p_first % T2, dc, ds, &S.bar_d);
+    // the down items stage h in the range of x and of the gate/up weights: a fill's bulk
+    // stores must have read wc / ws first (the down item's barrier orders the other
+    // threads after this wait)
+    if (tid == 0) bulk_wait_read();
     // the y tiles of this CTA's down items are zeroed (acquire: the adds come after)
     if (warp == 0) {
         int timeout = 0;
