@@ -880,11 +880,19 @@ def prefill_mx_leg(args, ft, wlm, world):
         barrier(world)
         ms_all.append(max_over_ranks(e0.elapsed_time(e1), world))
     status = ft.ft_cache_status(cache.handle)
+    ft.ft_profile_enable(cache.handle, True)           # per-kernel times of one more chunk
+    ft.ft_profile_read(cache.handle)
+    chunk()
+    torch.cuda.synchronize()
+    prof = ft.ft_profile_read(cache.handle)
+    ft.ft_profile_enable(cache.handle, False)
     cache.close()
     pool.free()
     ms = statistics.median(ms_all)
     link_ms = L * s.E * rec / (b_p * 1e9) * 1e3
+    per_layer = {k: v[0] / L for k, v in prof.items() if v[1]}
     return {"record_format": "mxfp4", "record_bytes": rec, "ms_per_chunk": ms,
+            "ms_per_layer_by_kind": per_layer,
             "tok_s": T * world / (ms / 1e3), "repeats_ms": [round(v, 2) for v in ms_all],
             "link_ms": link_ms, "frac": link_ms / ms, "b_p_gbs": b_p, "device_status": status}
 

@@ -122,10 +122,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16]) {
 // range and *bad set.
 __device__ __forceinline__ uint32_t e8m0_to_ue4m3(uint32_t c, int* bad) {
     const int k = (int)c - 127;
-    if (k >= -6 && k <= 8) return (uint32_t)(k + 7) << 3;
-    if (k >= -9 && k < -6) return 1u << (k + 9);
-    *bad = 1;
-    return k > 8 ? 0x78u : 0x01u;
+    const int kc = min(max(k, -9), 8);
+    *bad |= k != kc;
+    return kc >= -6 ? (uint32_t)(kc + 7) << 3 : 1u << (kc + 9);
 }
 
 struct TileInfo {
@@ -208,32 +207,49 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 uint8_t* sfa = st + kSA + kSB;
                 uint8_t* sfb = sfa + kSFA;
-                const int srow = g.K / 16;       // scale bytes per row
-                for (int r = lane; r < kBM; r += 32) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    const int row = ti.m0 + r;
-                    if (row < g.R_max)
-                        v = *reinterpret_cast<const uint4*>(g.a_scales + (size_t)row * srow + ks * 16);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                const int srow = g.K / 16;       // scale bytes per row (activations, NVFP4 B)
+                // every scale load of the stage goes out first (4 A rows and 8 B rows per
+                // lane in flight), then the 512-byte atoms are written
+                uint4 av[kBM / 32], bv[kBN / 32];
+#pragma unroll
+                for (int j = 0; j < kBM / 32; ++j) {
+                    const int row = ti.m0 + lane + 32 * j;
+                    av[j] = row < g.R_max
+                                ? __ldg(reinterpret_cast<const uint4*>(g.a_scales + (size_t)row * srow + ks * 16))
+                                : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int j = 0; j < kBN / 32; ++j) {
+                    const int n = lane + 32 * j;
+                    const int brow = g.kind == 1 ? (n < 128 ? ti.nt * 128 + n : g.I + ti.nt * 128 + (n - 128))
+                                                 : ti.nt * kBN + n;
+                    if (!g.mx) {
+                        bv[j] = __ldg(reinterpret_cast<const uint4*>(rec + g.off_b_scales + (size_t)brow * srow +
+                                                                     ks * 16));
+                    } else {                      // 8 E8M0 scales of 32 elements
+                        const uint2 v = __ldg(reinterpret_cast<const uint2*>(rec + g.off_b_scales +
+                                                                             (size_t)brow * (g.K / 32) + ks * 8));
+                        bv[j] = make_uint4(v.x, v.y, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBM / 32; ++j) {
+                    const int r = lane + 32 * j;
+                    const uint32_t w4[4] = {av[j].x, av[j].y, av[j].z, av[j].w};
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb)
                         *reinterpret_cast<uint32_t*>(sfa + kb * 512 + (r & 31) * 16 + (r >> 5) * 4) = w4[kb];
                 }
-                for (int n = lane; n < kBN; n += 32) {
-                    const int brow = g.kind == 1 ? (n < 128 ? ti.nt * 128 + n : g.I + ti.nt * 128 + (n - 128))
-                                                 : ti.nt * kBN + n;
+#pragma unroll
+                for (int j = 0; j < kBN / 32; ++j) {
+                    const int n = lane + 32 * j;
                     uint32_t w4[4];
                     if (!g.mx) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(rec + g.off_b_scales +
-                                                                        (size_t)brow * srow + ks * 16);
-                        w4[0] = v.x; w4[1] = v.y; w4[2] = v.z; w4[3] = v.w;
-                    } else {
-                        // 8 E8M0 scales of 32 elements -> 16 UE4M3 scales of 16 (each twice)
-                        const uint2 v = *reinterpret_cast<const uint2*>(rec + g.off_b_scales +
-                                                                        (size_t)brow * (g.K / 32) + ks * 8);
+                        w4[0] = bv[j].x; w4[1] = bv[j].y; w4[2] = bv[j].z; w4[3] = bv[j].w;
+                    } else {                      // -> 16 UE4M3 scales of 16 (each twice)
 #pragma unroll
                         for (int kb = 0; kb < 4; ++kb) {
-                            const uint32_t word = kb < 2 ? v.x : v.y;
+                            const uint32_t word = kb < 2 ? bv[j].x : bv[j].y;
                             const uint32_t s0 = e8m0_to_ue4m3((word >> (16 * (kb & 1))) & 0xFF, &scale_bad);
                             const uint32_t s1 = e8m0_to_ue4m3((word >> (16 * (kb & 1) + 8)) & 0xFF, &scale_bad);
                             w4[kb] = s0 | (s0 << 8) | (s1 << 16) | (s1 << 24);
