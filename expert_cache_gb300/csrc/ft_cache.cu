@@ -29,7 +29,6 @@ WsLayout ws_layout(const ft_cache_desc& d) {
     w.scalars = take(sizeof(DevScalars));
     w.sync = take(kSyncWords * 4);
     w.h = take(P * (size_t)d.I * 8);
-    w.hflag = take((R + 1) * (size_t)(d.I / decode_pairs(d.H)) * 8);
     w.yflag = take((size_t)(d.H / decode_rows(d.I)) * 8);
     w.h_end = w.yflag + (size_t)(d.H / decode_rows(d.I)) * 8;
     if (d.T_max > 0) {
@@ -399,7 +398,6 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
                                counters);
     a.h = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.h);
     a.sync = reinterpret_cast<unsigned*>(c->workspace + c->ws.sync);
-    a.hflag = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.hflag);
     a.yflag = reinterpret_cast<unsigned long long*>(c->workspace + c->ws.yflag);
     a.scrub = a.h;
     a.scrub_words = (c->ws.h_end - c->ws.h) / 8;

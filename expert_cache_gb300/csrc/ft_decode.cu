@@ -48,10 +48,10 @@
 // of this call holds, all within its first B*k positions.
 //
 // Exchange inside the grid: h values travel as single 64-bit words (call tag << 32
-// | fp32 bits), stored and loaded with relaxed gpu-scope accesses.  Each gate/up
-// item raises a flag word (the tag) after a CTA barrier; a down item has one warp
-// wait for its unit's flags, then reads h, re-polling any word whose store has not
-// landed yet.  Loads go out 8 at a time.  No fence or counter sits between those
+// | fp32 bits), stored and loaded with relaxed gpu-scope accesses.  A down item reads
+// its unit's h words directly, re-polling any word that does not carry the call's tag
+// yet (its gate/up item has not stored it); loads go out 8 at a time.  A per-item
+// flag to wait on first cost a round trip more.  No fence or counter sits between those
 // producers and consumers; the y tile flags (zeroed data in other words) are the one
 // release / acquire pair.  The tag is the
 // low half of a 64-bit call epoch kept in the scratch (never 0); every 2^31 calls
@@ -857,16 +857,6 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, const Decision& D,
         S.uw[threadIdx.x] = wsum;
     }
     int timeout = 0;
-    // the unit's gate/up items have all raised their flags ...
-    const int T1 = I / decode_pairs(a.H);
-    if ((threadIdx.x >> 5) == 0) {
-        const unsigned long long* f = a.hflag + (size_t)u * T1;
-        for (int j0 = threadIdx.x; j0 < T1; j0 += 8 * 32) {
-            float unused[8];
-            fetch_tagged<8>([&](int i) { return j0 + i * 32 < T1 ? f + j0 + i * 32 : nullptr; }, tag,
-                          unused, &timeout);
-        }
-    }
     __syncthreads();
     const bool landed = mbar_wait(&S.bar_d, par_d);
     if (!landed) timeout = 1;
@@ -875,7 +865,8 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, const Decision& D,
     const int ntok = __popc(tokmask);
     for (int g0 = 0; g0 < ntok; g0 += kTok) {
         const int ntg = min(kTok, ntok - g0);
-        // ... so h is there (a word whose store is still in flight is polled)
+        // the unit's h: every word carries the call's tag, so a word not yet written by
+        // its gate/up item (an older tag) is polled until it is
         const int ne = ntg * I;
         for (int e0 = threadIdx.x; e0 < ne; e0 += 8 * kThreads) {
             float v[8];
@@ -1316,12 +1307,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
         // ---- every 2^31 calls: zero the scratch words this call does not use
         if ((S.tag & 0x7fffffffu) == 1u) {
             const unsigned long long* h_end = a.h + (size_t)S.n_pairs * a.I;
-            const unsigned long long* hf_end = a.hflag + (size_t)n_units * (a.I / decode_pairs(a.H));
             const unsigned long long* yf_end = a.yflag + (n_units > 0 ? a.H / decode_rows(a.I) : 0);
             for (size_t i = tid; i < a.scrub_words; i += kThreads) {
                 unsigned long long* w = a.scrub + i;
-                const bool used = (w >= a.h && w < h_end) || (w >= a.yflag && w < yf_end) ||
-                                  (w >= a.hflag && w < hf_end);
+                const bool used = (w >= a.h && w < h_end) || (w >= a.yflag && w < yf_end);
                 if (!used) *w = 0ull;
             }
         }
@@ -1368,7 +1357,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
             prefetch_due = false;
         }
         gate_up_item(a, S, xs, wc, ws, par_w, ur, tile, D.u_pair0[u], D.u_mask[u], staged_all);
-        if (tid == 0) st_relaxed_u64(a.hflag + (size_t)u * T1 + tile, tagged(0.f, S.tag));
     }
     if (prefetch_due) prefetch_down(a, D, q, n_routed, p_first / T2, p_first % T2, dc, ds, &S.bar_d);
     // the down items stage h in the range of x and of the gate/up weights: a fill's bulk

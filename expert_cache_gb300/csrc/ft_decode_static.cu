@@ -7,7 +7,7 @@
 // loop that must never enter the CUDA allocator (an allocation can synchronise the
 // device and stall the token pipeline).  Such a caller still owns the cache (its
 // tables live in the workspace given to ft_cache_create) and passes inputs and
-// outputs; only the per-call scratch (the h activations, the per-item and per-tile
+// outputs; only the per-call scratch (the h activations, the per-tile
 // flags and the grid state of the decode kernel) comes from the static array below.
 //
 // The array is a module-scope __device__ object: every GPU that loads this
@@ -76,8 +76,6 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     size_t off = 0;
     const size_t o_sync = off;   off = up256(off + kSyncWords * 4);
     const size_t o_h = off;      off = up256(off + P * (size_t)c->d.I * 8);
-    const size_t U = (size_t)B * k + 1;                 // units of this call: <= B*k + shared
-    const size_t o_hf = off;     off = up256(off + U * (size_t)(c->d.I / decode_pairs(c->d.H)) * 8);
     const size_t o_yf = off;     off = up256(off + (size_t)(c->d.H / decode_rows(c->d.I)) * 8);
     if (off > kStaticScratchBytes)
         return fail(FT_ERR_ARG, "B, k, H and I need more than the 8 MiB static scratch");
@@ -96,7 +94,6 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
                                counters);
     a.h = reinterpret_cast<unsigned long long*>(scr + o_h);
     a.sync = reinterpret_cast<unsigned*>(scr + o_sync);
-    a.hflag = reinterpret_cast<unsigned long long*>(scr + o_hf);
     a.yflag = reinterpret_cast<unsigned long long*>(scr + o_yf);
     a.scrub = reinterpret_cast<unsigned long long*>(scr + o_h);
     a.scrub_words = (kStaticScratchBytes - o_h) / 8;

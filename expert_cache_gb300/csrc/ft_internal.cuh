@@ -88,7 +88,7 @@ struct DevScalars {
 // Offsets of the workspace regions (bytes, 256-aligned).
 struct WsLayout {
     size_t slot_for_id, id_of_slot, usage, lru_order, scalars;
-    size_t sync, h, hflag, yflag, h_end;   // decode grid state; tagged words (h_end: end)
+    size_t sync, h, yflag, h_end;   // decode grid state; tagged words (h_end: end)
     // prefill region (present when T_max > 0)
     size_t pf_chunk_cnt, pf_offsets, pf_mtile, pf_perm, pf_route_pos;
     size_t pf_a_codes, pf_a_scales, pf_h_codes, pf_h_scales, pf_o;
@@ -111,7 +111,6 @@ struct DecodeArgs {
     int32_t* lru_order;
     DevScalars* sc;
     unsigned long long* h; // [pairs, I] tagged values (tag << 32 | fp32 bits)
-    unsigned long long* hflag;  // [R_cap + 1, I / decode_pairs(H)] gate/up item done (tag)
     unsigned long long* yflag;  // [H / decode_rows(I)] y row tile zeroed (tag)
     unsigned* sync;        // kSyncWords words of grid state, 8-byte aligned
     unsigned long long* scrub;  // the whole h / o region of this call's scratch ...

@@ -180,9 +180,9 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
  * call before any stream capture.  Every call shares the array: calls that
  * overlap on the GPU race and must be serialised by the caller.  Errors: those of
  * ft_moe_decode, and FT_ERR_ARG when B, k, H and I need more than 8 MiB of scratch:
- * (B*k + B) * I * 8 bytes of h words, (B*k + 1) * (I / pairs) * 8 bytes of item flags
- * and (H / rows) * 8 bytes of tile flags, each region rounded up to 256 bytes, plus
- * 256 bytes of grid state (pairs = 16 and rows = 64 at the benchmark shapes). */
+ * (B*k + B) * I * 8 bytes of h words and (H / rows) * 8 bytes of tile flags, each
+ * region rounded up to 256 bytes, plus 256 bytes of grid state (rows = 64 at the
+ * benchmark shapes). */
 ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
                                const int32_t* topk_ids, const float* topk_w, int32_t B,
                                int32_t k, float* y, int32_t* deferred, int32_t* route_slot,
