@@ -24,6 +24,7 @@ FT_SPLIT_FULL_OFFLOAD, FT_SPLIT_QSTAR = 0, 1
 FT_PREFILL_DOUBLE_BUFFER = 1
 FT_PREFILL_DEBUG_X = 2
 FT_PREFILL_ON_DEMAND = 4
+FT_BACKEND_OFFLOAD, FT_BACKEND_HYBRID = 0, 1
 FT_PROF_KINDS = 5
 PROF_NAMES = ("decode", "prefill_gemm1", "prefill_gemm2", "prefill_other", "prefill_copy")
 
@@ -47,6 +48,19 @@ class FtCacheDesc(ctypes.Structure):
                 ("capacity_max", c_int32), ("T_max", c_int32),
                 ("host_pool", c_void_p), ("slot_buf", c_void_p), ("workspace", c_void_p),
                 ("shared_experts", c_void_p), ("split", FtSplit), ("format", c_int32)]
+
+
+class FtHostDesc(ctypes.Structure):
+    _fields_ = [("L", c_int32), ("E", c_int32), ("H", c_int32), ("I", c_int32),
+                ("k_max", c_int32), ("B_max", c_int32), ("format", c_int32),
+                ("host_pool", c_void_p), ("n_threads", c_int32), ("cpus", c_void_p),
+                ("mailbox", c_void_p)]
+
+
+class FtBwProfile(ctypes.Structure):
+    _fields_ = [("pcie_gbs", c_double), ("cpu_gbs", c_double), ("pcie_ov_gbs", c_double),
+                ("cpu_ov_gbs", c_double), ("recommend", c_int32), ("f_q16", c_uint32),
+                ("n_records", c_int32)]
 
 
 def _sig(name, res, *args):
@@ -96,6 +110,17 @@ _f = {
                            _P(c_double)),
     "ft_profile_enable": _sig("ft_profile_enable", c_int32, c_void_p, c_int32),
     "ft_profile_read": _sig("ft_profile_read", c_int32, c_void_p, _P(c_double), _P(c_int64)),
+    "ft_host_mailbox_bytes": _sig("ft_host_mailbox_bytes", c_int32, c_int32, c_int32, c_int32,
+                                  _P(c_size_t)),
+    "ft_host_branch_create": _sig("ft_host_branch_create", c_int32, _P(FtHostDesc), _P(c_void_p)),
+    "ft_host_branch_destroy": _sig("ft_host_branch_destroy", None, c_void_p),
+    "ft_host_moe": _sig("ft_host_moe", c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                        c_int32, c_void_p),
+    "ft_host_branch_stats": _sig("ft_host_branch_stats", c_int32, c_void_p, _P(c_int64), _P(c_int64)),
+    "ft_cache_set_host_branch": _sig("ft_cache_set_host_branch", c_int32, c_void_p, c_void_p),
+    "ft_profile_bandwidth": _sig("ft_profile_bandwidth", c_int32, c_void_p, c_void_p, c_int32,
+                                 c_void_p, _P(FtBwProfile)),
+    "ft_recommend_backend": _sig("ft_recommend_backend", c_int32, c_double, c_double),
     "ft_status_string": _sig("ft_status_string", ctypes.c_char_p, c_int32),
     "ft_last_error": _sig("ft_last_error", ctypes.c_char_p, c_void_p),
 }
@@ -295,6 +320,46 @@ def ft_profile_read(handle):
     return {PROF_NAMES[i]: (ms[i], n[i]) for i in range(FT_PROF_KINDS)}
 
 
+def ft_host_mailbox_bytes(H, k_max, B_max):
+    n = c_size_t()
+    _check(_f["ft_host_mailbox_bytes"](H, k_max, B_max, ctypes.byref(n)))
+    return n.value
+
+
+def ft_host_branch_create(desc: FtHostDesc):
+    h = c_void_p()
+    _check(_f["ft_host_branch_create"](ctypes.byref(desc), ctypes.byref(h)))
+    return h.value
+
+
+def ft_host_branch_destroy(hb):
+    _f["ft_host_branch_destroy"](hb)
+
+
+def ft_host_moe(hb, x, deferred, w, B, k, y):
+    _check(_f["ft_host_moe"](hb, _ptr(x), _ptr(deferred), _ptr(w), B, k, _ptr(y)))
+
+
+def ft_host_branch_stats(hb):
+    jobs, mb = c_int64(), c_int64()
+    _check(_f["ft_host_branch_stats"](hb, ctypes.byref(jobs), ctypes.byref(mb)))
+    return jobs.value, mb.value
+
+
+def ft_cache_set_host_branch(handle, hb):
+    _check(_f["ft_cache_set_host_branch"](handle, hb), handle)
+
+
+def ft_profile_bandwidth(handle, hb, n_records, stream=None):
+    out = FtBwProfile()
+    _check(_f["ft_profile_bandwidth"](handle, hb, n_records, _stream(stream), ctypes.byref(out)), handle)
+    return {k: getattr(out, k) for k, _ in FtBwProfile._fields_}
+
+
+def ft_recommend_backend(cpu_gbs, pcie_gbs):
+    return _f["ft_recommend_backend"](cpu_gbs, pcie_gbs)
+
+
 # ----------------------------------------------------------------- memory plumbing
 
 class PinnedBuffer:
@@ -349,6 +414,34 @@ class ExpertCache:
         if self.handle:
             ft_cache_destroy(self.handle)
             self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HostBranch:
+    """Owns one host branch (ft_host_branch_create) and its pinned mailbox."""
+
+    def __init__(self, L, E, H, I, k_max, B_max, host_pool_ptr, n_threads, cpus=None, fmt="nvfp4",
+                 mailbox=True):
+        self.H = H
+        self.mailbox = PinnedBuffer(ft_host_mailbox_bytes(H, k_max, B_max)) if mailbox else None
+        self._cpus = (ctypes.c_int32 * n_threads)(*cpus) if cpus is not None else None
+        self.desc = FtHostDesc(L, E, H, I, k_max, B_max, FORMATS[fmt], host_pool_ptr, n_threads,
+                               ctypes.addressof(self._cpus) if self._cpus is not None else None,
+                               self.mailbox.ptr if self.mailbox else None)
+        self.handle = ft_host_branch_create(self.desc)
+
+    def close(self):
+        if self.handle:
+            ft_host_branch_destroy(self.handle)
+            self.handle = None
+        if self.mailbox is not None:
+            self.mailbox.free()
+            self.mailbox = None
 
     def __del__(self):
         try:

@@ -12,6 +12,9 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libft.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+# host-only sources (the CPU branch): the host C++ compiler, no contraction of a*b+c
+# into fused operations beyond the ones the code writes out
+CXXFLAGS = ["-O3", "-std=c++17", "-fPIC", "-pthread", "-ffp-contract=off"]
 
 
 def _nvcc() -> str:
@@ -29,21 +32,24 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + sorted(glob.glob(os.path.join(CSRC, "*.cpp")))
+    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
         os.path.join(HERE, "..", "include", "ft.h")]
     nvcc = _nvcc()
     extra = list(extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         if _stale(obj, [src] + headers + [__file__]):
-            cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+            if src.endswith(".cpp"):
+                cmd = [os.environ.get("CXX", "c++"), *CXXFLAGS, "-c", src, "-o", obj]
+            else:
+                cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
                 print(" ".join(cmd), flush=True)
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
-                raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+                raise RuntimeError(f"compile failed on {src}:\n{r.stdout}\n{r.stderr}")
             if verbose and r.stderr:
                 print(r.stderr, flush=True)
         return obj
@@ -51,7 +57,7 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     with ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
         objs = list(ex.map(compile_one, sources))
     if _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB, *objs]
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB, *objs, "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -8,7 +8,9 @@
 #include <atomic>
 #include <new>
 
+#include <vector>
 #include "ft_internal.cuh"
+#include "ft_prefill.cuh"
 #include "ft_umma.cuh"
 
 namespace ft {
@@ -145,6 +147,12 @@ DecodeArgs decode_args(ft_cache* c, int layer, const void* x, const int32_t* ids
     a.counters = counters;
     a.trace = static_cast<unsigned long long*>(c->trace);
     a.trace_cap = c->trace ? (unsigned)c->trace_cap : 0u;
+    if (c->host) {
+        a.mb = c->mb_dev;
+        a.mb_x = (unsigned)c->ml.x;
+        a.mb_def = (unsigned)c->ml.def;
+        a.mb_w = (unsigned)c->ml.w;
+    }
     return a;
 }
 
@@ -230,6 +238,8 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
     c->prof_n = 0;
     c->trace = nullptr;
     c->trace_cap = 0;
+    c->host = nullptr;
+    c->mb_dev = nullptr;
     c->err[0] = 0;
     c->grid_decode = decode_grid(d->H, d->I, d->E, d->B_max * d->k_max);
     if (c->grid_decode < 2) {
@@ -402,8 +412,10 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
     a.scrub = a.h;
     a.scrub_words = (c->ws.h_end - c->ws.h) / 8;
     const int p = prof_begin(c, 0, s);
-    const cudaError_t e = launch_decode(a, c->grid_decode, s);
+    cudaError_t e = launch_decode(a, c->grid_decode, s);
     prof_end(c, p, s);
+    if (e == cudaSuccess && c->host)
+        e = launch_host_join(c->mb_dev, (unsigned)c->ml.y, y, B * c->d.H, &a.sc->status, s);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
     return FT_OK;
 }
@@ -506,6 +518,122 @@ ft_status ft_cache_set_trace(ft_cache* c, void* ring, int32_t capacity) {
     if (ring && !aligned(ring, 16)) return fail(c, FT_ERR_ARG, "trace ring must be 16-byte aligned");
     c->trace = capacity > 0 ? ring : nullptr;
     c->trace_cap = c->trace ? capacity : 0;
+    return FT_OK;
+}
+
+ft_status ft_cache_set_host_branch(ft_cache* c, ft_host_branch* hb) {
+    if (!c) return FT_ERR_ARG;
+    cudaError_t e = cudaDeviceSynchronize();   // no call of c still publishing to the old branch
+    if (e != cudaSuccess) return cuda_fail(c, e, "host branch attach");
+    if (!hb) {
+        c->host = nullptr;
+        c->mb_dev = nullptr;
+        return FT_OK;
+    }
+    ft::HostBranchInfo hi;
+    if (!ft::host_branch_info(hb, &hi)) return fail(c, FT_ERR_ARG, "host branch");
+    if (hi.pool != c->d.host_pool || hi.L != c->d.L || hi.E != c->d.E || hi.H != c->d.H || hi.I != c->d.I ||
+        hi.format != c->d.format || hi.B_max < c->d.B_max || hi.k_max < c->d.k_max || !hi.mailbox)
+        return fail(c, FT_ERR_ARG, "host branch of another pool, shape or format, or without a mailbox");
+    void* dev = nullptr;
+    e = cudaHostGetDevicePointer(&dev, hi.mailbox, 0);
+    if (e != cudaSuccess) return cuda_fail(c, e, "mailbox is not mapped pinned memory");
+    c->mb_dev = static_cast<uint8_t*>(dev);
+    c->ml = ft::mailbox_layout(hi.H, hi.k_max, hi.B_max);
+    c->host = hb;
+    return FT_OK;
+}
+
+int32_t ft_recommend_backend(double cpu_gbs, double pcie_gbs) {
+    return cpu_gbs > 2.0 * pcie_gbs ? FT_BACKEND_HYBRID : FT_BACKEND_OFFLOAD;
+}
+
+ft_status ft_profile_bandwidth(ft_cache* c, ft_host_branch* hb, int32_t n, void* stream, ft_bw_profile* out) {
+    NvtxRange range("ft_profile_bandwidth");
+    if (!c) return FT_ERR_ARG;
+    if (!hb || !out) return fail(c, FT_ERR_ARG, "NULL argument");
+    ft::HostBranchInfo hi;
+    if (!ft::host_branch_info(hb, &hi) || hi.pool != c->d.host_pool || hi.H != c->d.H || hi.I != c->d.I ||
+        hi.format != c->d.format || hi.L != c->d.L || hi.E != c->d.E)
+        return fail(c, FT_ERR_ARG, "host branch of another pool or shape");
+    if (n < 1 || n > c->C || n > c->d.L * c->d.E) return fail(c, FT_ERR_ARG, "n_records outside [1, min(C, L*E)]");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cuda_fail(c, cudaGetLastError(), "capture query");
+    if (cs != cudaStreamCaptureStatusNone) return fail(c, FT_ERR_STATE, "profile while capturing");
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->copy_stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "profile drain");
+    // the GPU fill path: records 0..n-1 gathered into slots 0..n-1
+    std::vector<int32_t> lists(2 * (size_t)n + 4);
+    for (int i = 0; i < n; ++i) { lists[i] = i; lists[n + i] = i; }
+    lists[2 * n] = n;
+    int32_t* dv = nullptr;
+    e = cudaMalloc(&dv, lists.size() * 4);
+    if (e != cudaSuccess) return cuda_fail(c, e, "profile lists");
+    ft::PrefillGatherArgs ga{};
+    ga.host_pool = c->host_pool_dev;
+    ga.slot_buf = c->slot_buf;
+    ga.rec_bytes = c->rec.bytes;
+    ga.fill_flat = dv;
+    ga.fill_slot = dv + n;
+    ga.n_fill = dv + 2 * n;
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    float ms = 0.f;
+    double t_p = 0, t_c = 0, t_pov = 0, t_cov = 0;
+    int reps = 1;
+    const double bytes = (double)n * (double)c->rec.bytes;
+    e = cudaMemcpy(dv, lists.data(), lists.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaEventCreate(&ev[0]);
+    if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
+    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, s);          // warm-up
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0], s);
+    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(ev[1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+    t_p = ms / 1e3;
+    // the host branch alone (one warm-up run)
+    if (e == cudaSuccess) {
+        ft::host_branch_run_flats(hb, lists.data(), n);
+        t_c = ft::host_branch_run_flats(hb, lists.data(), n);
+        if (t_c <= 0) e = cudaErrorInvalidValue;
+    }
+    // both together: enough gathers to cover the host run
+    if (e == cudaSuccess) {
+        reps = (int)std::max(1.0, std::min(64.0, std::round(t_c / std::max(t_p, 1e-9))));
+        e = cudaEventRecord(ev[0], s);
+        for (int r = 0; r < reps && e == cudaSuccess; ++r) e = ft::launch_pf_gather(ga, s);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+    }
+    if (e == cudaSuccess) {
+        t_cov = ft::host_branch_run_flats(hb, lists.data(), n);
+        e = cudaEventSynchronize(ev[1]);
+    }
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+    t_pov = ms / 1e3 / reps;
+    for (auto v : ev) if (v) cudaEventDestroy(v);
+    cudaFree(dv);
+    // the gathers overwrote slots 0..n-1 behind the tables: empty the cache
+    if (e == cudaSuccess) {
+        uint8_t* ws = c->workspace;
+        c->buffer_layer[0] = c->buffer_layer[1] = -1;
+        e = launch_init_tables(reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id), c->d.L * c->d.E,
+                               reinterpret_cast<int32_t*>(ws + c->ws.id_of_slot),
+                               reinterpret_cast<long long*>(ws + c->ws.usage),
+                               reinterpret_cast<int32_t*>(ws + c->ws.lru_order), c->C,
+                               reinterpret_cast<DevScalars*>(ws + c->ws.scalars), false, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "bandwidth profile");
+    out->n_records = n;
+    out->pcie_gbs = bytes / t_p / 1e9;
+    out->cpu_gbs = bytes / t_c / 1e9;
+    out->pcie_ov_gbs = bytes / t_pov / 1e9;
+    out->cpu_ov_gbs = t_cov > 0 ? bytes / t_cov / 1e9 : 0.0;
+    out->recommend = ft_recommend_backend(out->cpu_gbs, out->pcie_gbs);
+    out->f_q16 = ft_split_from_overlap(out->pcie_ov_gbs, out->cpu_ov_gbs);
     return FT_OK;
 }
 

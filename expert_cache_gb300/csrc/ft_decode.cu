@@ -65,6 +65,7 @@
 // products are exact and accumulate in fp32 (fma.rn.f32.f16); each 16-element block
 // partial is scaled by its E4M3 scale in fp32; the fp32 tensor scale and the
 // prescale are applied at the end.  h stays fp32; the down GEMV is fp32 FMA.
+#include <algorithm>
 #include <mutex>
 
 #include "ft_internal.cuh"
@@ -1248,6 +1249,39 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
                 rec->t_commit_ns = (long long)gtime();
             }
         }
+        // ---- the host share to the host branch: deferred ids, gates and x into its
+        // mailbox (device-mapped pinned memory), then the task flag with a system-scope
+        // release after every writer's fence; done is cleared first, so the join kernel
+        // of this call waits for this call's partial
+        if (a.mb) {
+            MailboxHeader* hd = reinterpret_cast<MailboxHeader*>(a.mb);
+            const int nd = S.n_def;
+            if (nd > 0) {
+                int32_t* mdef = reinterpret_cast<int32_t*>(a.mb + a.mb_def);
+                float* mw = reinterpret_cast<float*>(a.mb + a.mb_w);
+                for (int r = tid; r < R; r += kThreads) {
+                    mdef[r] = D.r_unit[r] == -1 ? base_id + a.ids[r] : -1;
+                    mw[r] = a.w[r];
+                }
+                const uint4* xs = reinterpret_cast<const uint4*>(a.x);
+                uint4* xd = reinterpret_cast<uint4*>(a.mb + a.mb_x);
+                for (int i = tid; i < B * a.H / 8; i += kThreads) xd[i] = xs[i];
+            }
+            if (tid == 0) {
+                hd->layer = a.layer;
+                hd->B = B;
+                hd->k = k;
+                hd->n_def = nd;
+                asm volatile("st.relaxed.sys.global.u32 [%0], 0;" :: "l"(&hd->done) : "memory");
+            }
+            __threadfence_system();
+            __syncthreads();
+            if (tid == 0 && nd > 0) {
+                hd->published += 1;
+                __threadfence_system();
+                asm volatile("st.release.sys.global.u32 [%0], 1;" :: "l"(&hd->task) : "memory");
+            }
+        }
         for (int i = tid; i < q; i += kThreads) v_old[i] = a.id_of_slot[D.u_s[i]];
         // touched slots: the hits' and the victims'
         for (int w = tid; w < nwC; w += kThreads) S.touched[w] = 0;
@@ -1436,6 +1470,44 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+}
+
+// ------------------------------------------------------------------ host share join
+
+// y += the host branch's partial of the call just decoded (mailbox in device-mapped
+// pinned memory), once the branch raised `done` (system-scope acquire; bounded wait of
+// one second, then FT_DEV_TIMEOUT and no add).  No host routes: nothing to wait for.
+__global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, int* status) {
+    __shared__ int go;
+    MailboxHeader* hd = reinterpret_cast<MailboxHeader*>(mb);
+    if (threadIdx.x == 0) {
+        int g = 0;
+        if (*reinterpret_cast<volatile int*>(&hd->n_def) > 0) {
+            unsigned v;
+            asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(&hd->done) : "memory");
+            if (v != 1u) {
+                const unsigned long long t0 = gtime();
+                for (unsigned it = 0; it < kWaitIters && v != 1u; ++it) {
+                    __nanosleep(128);
+                    asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(&hd->done) : "memory");
+                    if ((it & 63u) == 63u && gtime() - t0 > kWaitNs) break;
+                }
+            }
+            if (v == 1u) g = 1;
+            else if (blockIdx.x == 0) atomicOr(status, FT_DEV_TIMEOUT);
+        }
+        go = g;
+    }
+    __syncthreads();
+    if (!go) return;
+    const float* yh = reinterpret_cast<const float*>(mb + mb_y);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] += __ldcv(yh + i);
+}
+
+cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, int* status, cudaStream_t s) {
+    const int grid = std::min((n + 255) / 256, 64);
+    host_join_kernel<<<grid, 256, 0, s>>>(mb, mb_y, y, n, status);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ bounded waits check

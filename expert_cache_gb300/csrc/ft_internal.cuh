@@ -12,6 +12,8 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "../../include/ft.h"
+#include "ft_record.h"
+#include "ft_host.h"
 
 namespace ft {
 
@@ -53,28 +55,7 @@ inline int decode_rows(int I) {
 }
 
 // ----------------------------------------------------------------- record
-struct RecordLayout {
-    size_t gu_codes, gu_scales, d_codes, d_scales, s_gu, s_d;
-    size_t raw, bytes;
-};
-
-// Scale block length along K: 16 (NVFP4, E4M3 scales) or 32 (MXFP4, E8M0 scales).
-inline int scale_block(int format) { return format == FT_FORMAT_MXFP4 ? 32 : 16; }
-
-inline RecordLayout record_layout(int H, int I, int format = FT_FORMAT_NVFP4) {
-    RecordLayout r;
-    const size_t sb = (size_t)scale_block(format);
-    size_t off = 0;
-    r.gu_codes = off;  off += (size_t)2 * I * H / 2;
-    r.gu_scales = off; off += (size_t)2 * I * H / sb;
-    r.d_codes = off;   off += (size_t)H * I / 2;
-    r.d_scales = off;  off += (size_t)H * I / sb;
-    r.s_gu = off;      off += 4;
-    r.s_d = off;       off += 4;
-    r.raw = off;
-    r.bytes = (off + 255) / 256 * 256;
-    return r;
-}
+// (RecordLayout, scale_block, record_layout: ft_record.h)
 
 // ----------------------------------------------------------------- device state
 // Scalars kept in the workspace (device).
@@ -134,6 +115,8 @@ struct DecodeArgs {
     int32_t* counters;
     unsigned long long* trace;  // stats ring header (count), or nullptr
     unsigned trace_cap;         // records after the 16-byte header
+    uint8_t* mb;                // host branch mailbox (device-mapped), or nullptr
+    unsigned mb_x, mb_def, mb_w;  // its x, deferred-id and gate regions (byte offsets)
 };
 
 // Kernel launchers (each returns the launch error).
@@ -145,6 +128,9 @@ cudaError_t launch_init_tables(int32_t* slot_for_id, int n_ids, int32_t* id_of_s
 int decode_grid(int H, int I, int E, int R_cap);
 cudaError_t check_bounded_waits(unsigned* expired);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
+// After a decode call with a host branch: wait (bounded) for the branch's partial and
+// add it into y (fp32 [B, H]); sets FT_DEV_TIMEOUT in *status when the wait runs out.
+cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, int* status, cudaStream_t s);
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s);
 cudaError_t launch_quantize_mx(const float* w_gu, const float* w_d, int n, int H, int I,
@@ -243,6 +229,9 @@ struct ft_cache {
     int grid_decode;
     void* trace;                    // per-call stats ring (device) or nullptr
     int trace_cap;
+    ft_host_branch* host;           // attached host branch, or nullptr
+    uint8_t* mb_dev;                // its mailbox (device-mapped)
+    ft::MailboxLayout ml;
     // profiling
     unsigned prof;          // bit i set: time launches of kind i
     static constexpr int kProfEvents = 65536;

@@ -314,6 +314,84 @@ ft_status ft_profile_enable(ft_cache* c, int32_t kinds);
 ft_status ft_profile_read(ft_cache* c, double* total_ms /*[FT_PROF_KINDS]*/,
                           int64_t* launches /*[FT_PROF_KINDS]*/);
 
+/* ---- The host share of decode ([EXPLAINER §8.3]; [BWRATIO "代码全链路" §2]; [JUHE
+ * "为什么可以直接相加？"]).
+ * A host branch is a persistent pool of n_threads worker threads, each pinned to one
+ * CPU core, that computes routes left to the host (deferred >= 0) straight from the
+ * pinned pool: the same SwiGLU expert on the records' codes and scales, dequantised
+ * inside the GEMV (NEON on aarch64), with fp32 products and sums:
+ *   y[b] += w[b,j] * Expert_{deferred[b,j]}(x[b]) over the host routes, experts in
+ *   ascending flat id.
+ * Attached to a cache (ft_cache_set_host_branch), every decode call hands its host
+ * share to the branch right after its decision: the decode kernel writes the call's
+ * deferred ids, gates and x into the branch's mailbox (pinned, device-mapped) and
+ * raises a flag; worker 0 sees it, the workers compute the host partial into the
+ * mailbox while the GPU computes its own share, and a join kernel, launched on the
+ * call's stream right after the decode kernel, waits for the branch (bounded: one
+ * second, then FT_DEV_TIMEOUT) and adds the host partial into y.  y then holds the
+ * whole layer output y_gpu + y_cpu; a call with no host routes joins nothing.
+ * Both calls stay asynchronous and capturable; the branch's workers spin while calls
+ * arrive and back off when idle. */
+typedef struct ft_host_branch ft_host_branch;
+typedef struct {
+    int32_t L, E, H, I, k_max, B_max, format;   /* as the cache's descriptor */
+    const void* host_pool;   /* pinned pool (the cache's), L*E records */
+    int32_t n_threads;       /* workers, >= 1 */
+    const int32_t* cpus;     /* n_threads CPU ids to pin the workers to, or NULL: the
+                                first n_threads CPUs this process may run on */
+    void* mailbox;           /* pinned (ft_pinned_alloc), 256-byte aligned,
+                                ft_host_mailbox_bytes(H, k_max, B_max) bytes; NULL:
+                                the branch only serves ft_host_moe */
+} ft_host_desc;
+/* Bytes of a mailbox for hidden H, k_max, B_max.  FT_ERR_ARG on bad sizes. */
+ft_status ft_host_mailbox_bytes(int32_t H, int32_t k_max, int32_t B_max, size_t* bytes);
+/* Start a branch (threads created and pinned).  FT_ERR_ARG on bad fields. */
+ft_status ft_host_branch_create(const ft_host_desc* d, ft_host_branch** out);
+/* Stop and join the workers.  Detach the branch from every cache first. */
+void      ft_host_branch_destroy(ft_host_branch* hb);
+/* The host share of one call, computed now by the workers (synchronous; host memory):
+ *   x host bf16 [B, H]; deferred host int32 [B, k] flat ids (l*E + e) or -1;
+ *   w host fp32 [B, k]; y host fp32 [B, H], overwritten with the host partial.
+ * Not to be called while decode calls on an attached cache are in flight.
+ * Errors: FT_ERR_ARG (NULL pointer, B outside [1, B_max], k outside [1, k_max]). */
+ft_status ft_host_moe(ft_host_branch* hb, const void* x, const int32_t* deferred, const float* w,
+                      int32_t B, int32_t k, float* y);
+/* Jobs run by the branch (all, and those published by decode kernels). */
+ft_status ft_host_branch_stats(const ft_host_branch* hb, int64_t* jobs, int64_t* mailbox_jobs);
+/* Attach hb (or detach with NULL): later decode calls of c hand their host share to
+ * it and add its partial into y.  hb must describe c's shape, format and pool, with
+ * B_max and k_max at least the cache's, and have a mailbox.  Synchronises the cache's
+ * streams.  Errors: FT_ERR_ARG (mismatch), FT_ERR_CUDA. */
+ft_status ft_cache_set_host_branch(ft_cache* c, ft_host_branch* hb);
+
+/* ---- Bandwidth profile ([EXPLAINER §6.3]; [BWRATIO "第一层带宽比", "实测版本"];
+ * [QIITA §7]): the two real miss paths over the same n_records records of the pool
+ * (flat ids 0 .. n_records-1), in record bytes per second:
+ *   pcie_gbs      the GPU fill path alone: the records gathered from the pinned pool
+ *                 into slots 0 .. n_records-1 by the GPU's gather kernel;
+ *   cpu_gbs       the host branch alone: its workers computing one token through
+ *                 every record (ft_host_moe's GEMV);
+ *   pcie_ov_gbs, cpu_ov_gbs   both started together, each over its own duration.
+ * recommend = ft_recommend_backend(cpu_gbs, pcie_gbs); f_q16 =
+ * ft_split_from_overlap(pcie_ov_gbs, cpu_ov_gbs).  A safe-point call: synchronises,
+ * and leaves the cache empty (like ft_cache_resize to the same capacity); allocates
+ * and frees 8 * n_records + 16 bytes of device memory.  Errors: FT_ERR_ARG
+ * (n_records outside [1, min(C, L*E)], NULL pointers, a branch of another pool or
+ * shape), FT_ERR_STATE (capturing), FT_ERR_CUDA. */
+#define FT_BACKEND_OFFLOAD 0
+#define FT_BACKEND_HYBRID  1
+typedef struct {
+    double pcie_gbs, cpu_gbs, pcie_ov_gbs, cpu_ov_gbs;
+    int32_t recommend;
+    uint32_t f_q16;
+    int32_t n_records;
+} ft_bw_profile;
+ft_status ft_profile_bandwidth(ft_cache* c, ft_host_branch* hb, int32_t n_records, void* stream,
+                               ft_bw_profile* out);
+/* [BWRATIO "第一层带宽比"]: FT_BACKEND_HYBRID when the CPU expert path is more than
+ * twice as fast as the fill path (cpu_gbs > 2 * pcie_gbs), else FT_BACKEND_OFFLOAD. */
+int32_t   ft_recommend_backend(double cpu_gbs, double pcie_gbs);
+
 const char* ft_status_string(ft_status s);
 /* Message of the last failed call on c (static storage), or "" */
 const char* ft_last_error(const ft_cache* c);

@@ -16,6 +16,9 @@ Sources:
                         a tie; then cap at M.
   [QIITA §8]            latency(q) = max(q/B_P, (m-q)/(B_H-B_P)) and the 27.6 % loss
                         of naive rounding on the 5090 Desktop at m = 8.
+  [BWRATIO "第一层带宽比"]  the backend choice from the two measured bandwidths: the
+                        hybrid backend only when the CPU expert path is more than twice
+                        as fast as the fill path (ratio cpu/pcie > 2), else offload.
 
 Reading adopted where the pages differ: the [BWRATIO] Q16 rule, then the "at least
 one fill" clamp of [EXPLAINER §6.5] / [JUHE] "q*：为什么不是一半给 CPU、一半给 GPU",
@@ -83,3 +86,9 @@ def exposed_latency(q: int, m: int, b_p: float, b_h: float, s: float = 1.0) -> f
         return t_fill
     b_r = max(b_h - b_p, 0.0)
     return math.inf if b_r <= 0 else max(t_fill, (m - q) * s / b_r)
+
+
+def recommend_backend(cpu_gbs: float, pcie_gbs: float, threshold: float = 2.0) -> str:
+    """[BWRATIO "第一层带宽比"]: "hybrid" when cpu_gbs > threshold * pcie_gbs, else
+    "offload" (a ratio of exactly the threshold stays with offload)."""
+    return "hybrid" if cpu_gbs > threshold * pcie_gbs else "offload"
