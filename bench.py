@@ -362,11 +362,16 @@ def roofline_ms(cnt, hbm_gbs, b_p):
 class DecodeRun:
     """A decode workload over one cache: reset + warm-up + timed graph replays."""
 
-    def __init__(self, ft, wlm, s, pool_ptr, shared, split, seed, steps, fmt="nvfp4"):
+    def __init__(self, ft, wlm, s, pool_ptr, shared, split, seed, steps, fmt="nvfp4", host_threads=0):
         self.ft, self.s = ft, s
         self.cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool_ptr, shared=shared,
                                     split=split, capacity_max=max([s.C] + list(s.resize.values())),
                                     fmt=fmt)
+        self.host = None
+        if host_threads:
+            # the host share of every call computed by a pinned worker pool and joined into y
+            self.host = ft.HostBranch(s.L, s.E, s.H, s.I, s.k, s.B, pool_ptr, host_threads, fmt=fmt)
+            ft.ft_cache_set_host_branch(self.cache.handle, self.host.handle)
         self.wl = wlm.DecodeWorkload(s, seed=seed, steps=steps)
         self.graph = wlm.StepGraph(self.wl, self.cache)
         self.steps = steps
@@ -450,7 +455,30 @@ class DecodeRun:
         return e0.elapsed_time(e1), h2d, g.y.numel() * 4
 
     def close(self):
+        if self.host is not None:
+            self.ft.ft_cache_set_host_branch(self.cache.handle, None)
         self.cache.close()
+        if self.host is not None:
+            self.host.close()
+
+
+def bandwidth_profile(ft, s, pool, shared, n_threads, n_records=64):
+    """The two miss paths of this machine over n_records records of the pool: the GPU
+    gather (fill path) and the host branch's GEMV, alone and together; the backend rule
+    and the overlap split (ft_profile_bandwidth)."""
+    cache = ft.ExpertCache(s.L, s.E, s.H, s.I, s.k, s.B, s.C, pool.ptr, shared=shared)
+    hb = ft.HostBranch(s.L, s.E, s.H, s.I, s.k, s.B, pool.ptr, n_threads, mailbox=False)
+    prof = ft.ft_profile_bandwidth(cache.handle, hb.handle, n_records)
+    cache.close()
+    hb.close()
+    prof["host_threads"] = n_threads
+    prof["recommend"] = "hybrid" if prof["recommend"] == ft.FT_BACKEND_HYBRID else "offload"
+    prof["f_overlap"] = prof["f_q16"] / 65536
+    prof["ratio_cpu_over_pcie"] = prof["cpu_gbs"] / prof["pcie_gbs"]
+    prof["note"] = ("record bytes per second: pcie = GPU gather of the records from the pinned pool "
+                    "into slots, cpu = the host branch computing one token through each record; "
+                    "ov = both at once; hybrid iff cpu > 2 x pcie; f = pcie_ov / (pcie_ov + cpu_ov)")
+    return prof
 
 
 def measure_b_p(ft, pool, torch):
@@ -596,6 +624,20 @@ def native(args, rank, world):
                 legs[f"qwen_p{p}_{mode}"] = decode_leg(ft, wlm, sp, pool.ptr, shared, mode, f,
                                                        args.seed, 32, 256, rec_bytes, hbm_gbs,
                                                        b_p, world, stream)
+        # the host share computed as well (end to end), and the bandwidth profile that
+        # picks the backend and the split on this machine
+        n_host = max(1, cpu_cores() - 1)
+        for p in (0.5, 0.8):
+            sp = replace(s, p=p)
+            legs[f"qwen_p{p}_qstar_hybrid"] = decode_leg(ft, wlm, sp, pool.ptr, shared, "qstar", f_half,
+                                                         args.seed, 32, 256, rec_bytes, hbm_gbs, b_p,
+                                                         world, stream, host_threads=n_host)
+        bw = bandwidth_profile(ft, s, pool, shared, n_host)
+        out["bandwidth_profile"] = bw
+        sp = replace(s, p=0.8)
+        legs["qwen_p0.8_profiled_split_hybrid"] = decode_leg(
+            ft, wlm, sp, pool.ptr, shared, "qstar", max(1, bw["f_q16"]), args.seed, 32, 256, rec_bytes,
+            hbm_gbs, b_p, world, stream, host_threads=n_host)
         out["legs"] = legs
     del shared
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -608,15 +650,22 @@ def native(args, rank, world):
 
 
 def decode_leg(ft, wlm, s, pool_ptr, shared, mode, f_q16, seed, warmup, steps, rec_bytes,
-               hbm_gbs, b_p, world, stream, fmt="nvfp4"):
+               hbm_gbs, b_p, world, stream, fmt="nvfp4", host_threads=0):
     run = DecodeRun(ft, wlm, s, pool_ptr, shared, wlm.split_tuple(mode, f_q16), seed,
-                    warmup + steps, fmt=fmt)
+                    warmup + steps, fmt=fmt, host_threads=host_threads)
     ms = max_over_ranks(run.timed(warmup, world, stream), world)
     cnt = decode_counts(run.wl, warmup, warmup + steps, rec_bytes, s.shared)
     status = ft.ft_cache_status(run.cache.handle)
+    host = None
+    if run.host is not None:
+        jobs, mailbox_jobs = ft.ft_host_branch_stats(run.host.handle)
+        host = {"threads": host_threads, "calls_joined": mailbox_jobs,
+                "note": "y includes the host share: deferred routes computed by the host branch "
+                        "concurrently with the GPU share and added by the join kernel"}
     run.close()
     roof = roofline_ms(cnt, hbm_gbs, b_p)
-    return {"config": config_of(s, mode, f_q16, rec_bytes), "steps": steps, "warmup": warmup,
+    leg_out = {"host_branch": host} if host else {}
+    return {**leg_out, "config": config_of(s, mode, f_q16, rec_bytes), "steps": steps, "warmup": warmup,
             "tok_s": steps * s.B * world / (ms / 1e3), "ms_per_step": ms / steps,
             "roofline_ms_per_step": roof / steps, "frac": roof / ms,
             "hits_per_step": cnt["hits"] / steps, "misses_per_step": cnt["misses"] / steps,

@@ -1477,9 +1477,12 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
 // y += the host branch's partial of the call just decoded (mailbox in device-mapped
 // pinned memory), once the branch raised `done` (system-scope acquire; bounded wait of
 // one second, then FT_DEV_TIMEOUT and no add).  No host routes: nothing to wait for.
+// Launched as a programmatic dependent of the decode kernel: it is scheduled while the
+// decode kernel runs and starts its work when that kernel has completed.
 __global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, int* status) {
     __shared__ int go;
     MailboxHeader* hd = reinterpret_cast<MailboxHeader*>(mb);
+    pdl_wait_and_release();
     if (threadIdx.x == 0) {
         int g = 0;
         if (*reinterpret_cast<volatile int*>(&hd->n_def) > 0) {
@@ -1506,8 +1509,7 @@ __global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, in
 
 cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, int* status, cudaStream_t s) {
     const int grid = std::min((n + 255) / 256, 64);
-    host_join_kernel<<<grid, 256, 0, s>>>(mb, mb_y, y, n, status);
-    return cudaGetLastError();
+    return launch_pdl(host_join_kernel, dim3(grid), dim3(256), 0, s, mb, mb_y, y, n, status);
 }
 
 // ------------------------------------------------------------------ bounded waits check
