@@ -415,7 +415,7 @@ ft_status ft_moe_decode(ft_cache* c, int32_t layer, const void* x, const int32_t
     cudaError_t e = launch_decode(a, c->grid_decode, s);
     prof_end(c, p, s);
     if (e == cudaSuccess && c->host)
-        e = launch_host_join(c->mb_dev, (unsigned)c->ml.y, y, B * c->d.H, &a.sc->status, s);
+        e = launch_host_join(c->mb_dev, (unsigned)c->ml.y, y, B * c->d.H, &a.sc->counters[3], &a.sc->status, s);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
     return FT_OK;
 }

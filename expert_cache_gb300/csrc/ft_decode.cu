@@ -1249,38 +1249,34 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(DecodeArgs a)
                 rec->t_commit_ns = (long long)gtime();
             }
         }
-        // ---- the host share to the host branch: deferred ids, gates and x into its
-        // mailbox (device-mapped pinned memory), then the task flag with a system-scope
-        // release after every writer's fence; done is cleared first, so the join kernel
-        // of this call waits for this call's partial
-        if (a.mb) {
+        // ---- a call with host routes hands them to the host branch: deferred ids,
+        // gates and x into its mailbox (device-mapped pinned memory), then the task flag
+        // with a system-scope release after every writer's fence; done is cleared first,
+        // so the join kernel of this call waits for this call's partial.  A call without
+        // host routes touches no host memory (the join reads the count from the
+        // workspace).
+        if (a.mb && S.n_def > 0) {
             MailboxHeader* hd = reinterpret_cast<MailboxHeader*>(a.mb);
-            const int nd = S.n_def;
-            if (nd > 0) {
-                int32_t* mdef = reinterpret_cast<int32_t*>(a.mb + a.mb_def);
-                float* mw = reinterpret_cast<float*>(a.mb + a.mb_w);
-                for (int r = tid; r < R; r += kThreads) {
-                    mdef[r] = D.r_unit[r] == -1 ? base_id + a.ids[r] : -1;
-                    mw[r] = a.w[r];
-                }
-                const uint4* xs = reinterpret_cast<const uint4*>(a.x);
-                uint4* xd = reinterpret_cast<uint4*>(a.mb + a.mb_x);
-                for (int i = tid; i < B * a.H / 8; i += kThreads) xd[i] = xs[i];
+            int32_t* mdef = reinterpret_cast<int32_t*>(a.mb + a.mb_def);
+            float* mw = reinterpret_cast<float*>(a.mb + a.mb_w);
+            for (int r = tid; r < R; r += kThreads) {
+                mdef[r] = D.r_unit[r] == -1 ? base_id + a.ids[r] : -1;
+                mw[r] = a.w[r];
             }
+            const uint4* xs = reinterpret_cast<const uint4*>(a.x);
+            uint4* xd = reinterpret_cast<uint4*>(a.mb + a.mb_x);
+            for (int i = tid; i < B * a.H / 8; i += kThreads) xd[i] = xs[i];
             if (tid == 0) {
                 hd->layer = a.layer;
                 hd->B = B;
                 hd->k = k;
-                hd->n_def = nd;
+                hd->n_def = S.n_def;
+                hd->published += 1;
                 asm volatile("st.relaxed.sys.global.u32 [%0], 0;" :: "l"(&hd->done) : "memory");
             }
             __threadfence_system();
             __syncthreads();
-            if (tid == 0 && nd > 0) {
-                hd->published += 1;
-                __threadfence_system();
-                asm volatile("st.release.sys.global.u32 [%0], 1;" :: "l"(&hd->task) : "memory");
-            }
+            if (tid == 0) asm volatile("st.release.sys.global.u32 [%0], 1;" :: "l"(&hd->task) : "memory");
         }
         for (int i = tid; i < q; i += kThreads) v_old[i] = a.id_of_slot[D.u_s[i]];
         // touched slots: the hits' and the victims'
@@ -1476,16 +1472,19 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
 
 // y += the host branch's partial of the call just decoded (mailbox in device-mapped
 // pinned memory), once the branch raised `done` (system-scope acquire; bounded wait of
-// one second, then FT_DEV_TIMEOUT and no add).  No host routes: nothing to wait for.
-// Launched as a programmatic dependent of the decode kernel: it is scheduled while the
-// decode kernel runs and starts its work when that kernel has completed.
-__global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, int* status) {
+// one second, then FT_DEV_TIMEOUT and no add).  No host routes (*n_def, the call's
+// count in the workspace, is 0): nothing to wait for.  Launched as a programmatic
+// dependent of the decode kernel: it is scheduled while the decode kernel runs, lets
+// the next kernel on the stream be scheduled at once (that kernel waits for this one
+// to complete), and starts its work when the decode kernel has completed.
+__global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, const int* n_def, int* status) {
     __shared__ int go;
     MailboxHeader* hd = reinterpret_cast<MailboxHeader*>(mb);
-    pdl_wait_and_release();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
         int g = 0;
-        if (*reinterpret_cast<volatile int*>(&hd->n_def) > 0) {
+        if (*n_def > 0) {
             unsigned v;
             asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(&hd->done) : "memory");
             if (v != 1u) {
@@ -1507,9 +1506,10 @@ __global__ void host_join_kernel(uint8_t* mb, unsigned mb_y, float* y, int n, in
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] += __ldcv(yh + i);
 }
 
-cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, int* status, cudaStream_t s) {
+cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, const int* n_def, int* status,
+                             cudaStream_t s) {
     const int grid = std::min((n + 255) / 256, 64);
-    return launch_pdl(host_join_kernel, dim3(grid), dim3(256), 0, s, mb, mb_y, y, n, status);
+    return launch_pdl(host_join_kernel, dim3(grid), dim3(256), 0, s, mb, mb_y, y, n, n_def, status);
 }
 
 // ------------------------------------------------------------------ bounded waits check

@@ -101,7 +101,7 @@ extern "C" ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void
     cudaError_t e = launch_decode(a, c->grid_decode, s);
     prof_end(c, p, s);
     if (e == cudaSuccess && c->host)
-        e = launch_host_join(c->mb_dev, (unsigned)c->ml.y, y, B * c->d.H, &a.sc->status, s);
+        e = launch_host_join(c->mb_dev, (unsigned)c->ml.y, y, B * c->d.H, &a.sc->counters[3], &a.sc->status, s);
     if (e != cudaSuccess) {
         snprintf(c->err, sizeof(c->err), "static decode launch: %s", cudaGetErrorString(e));
         return FT_ERR_CUDA;

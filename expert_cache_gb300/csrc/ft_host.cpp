@@ -318,7 +318,8 @@ struct ft_host_branch {
         unsigned spins = 0;
         auto idle_since = std::chrono::steady_clock::now();
         while (!stop.load(std::memory_order_relaxed)) {
-            if (w == 0 && mailbox && __atomic_load_n(&header()->task, __ATOMIC_ACQUIRE) == 1u) {
+            // (the mailbox lives in memory the GPU writes: read it every 8th round only)
+            if (w == 0 && mailbox && (spins & 7u) == 0 && __atomic_load_n(&header()->task, __ATOMIC_ACQUIRE) == 1u) {
                 std::unique_lock<std::mutex> lk(job_mu, std::try_to_lock);
                 if (lk.owns_lock()) {
                     __atomic_store_n(&header()->task, 0u, __ATOMIC_RELAXED);

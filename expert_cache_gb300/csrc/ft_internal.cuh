@@ -128,9 +128,11 @@ cudaError_t launch_init_tables(int32_t* slot_for_id, int n_ids, int32_t* id_of_s
 int decode_grid(int H, int I, int E, int R_cap);
 cudaError_t check_bounded_waits(unsigned* expired);
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
-// After a decode call with a host branch: wait (bounded) for the branch's partial and
-// add it into y (fp32 [B, H]); sets FT_DEV_TIMEOUT in *status when the wait runs out.
-cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, int* status, cudaStream_t s);
+// After a decode call with a host branch: when the call had host routes (*n_def > 0),
+// wait (bounded) for the branch's partial and add it into y (fp32 [B, H]); sets
+// FT_DEV_TIMEOUT in *status when the wait runs out.
+cudaError_t launch_host_join(uint8_t* mb, unsigned mb_y, float* y, int n, const int* n_def, int* status,
+                             cudaStream_t s);
 cudaError_t launch_quantize(const float* w_gu, const float* w_d, int n, int H, int I,
                             uint8_t* records, size_t rec_bytes, cudaStream_t s);
 cudaError_t launch_quantize_mx(const float* w_gu, const float* w_d, int n, int H, int I,
