@@ -135,6 +135,10 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
     asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
 }
+// The same for two adjacent words (p 8-byte aligned): one request.
+__device__ __forceinline__ void red_add_v2_f32(float* p, float v0, float v1) {
+    asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" :: "l"(p), "f"(v0), "f"(v1) : "memory");
+}
 
 // One thread waits until *p >= target; false when the bound ran out.
 __device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target) {
@@ -670,6 +674,79 @@ __device__ void gate_up_rows(const DecodeArgs& a, const SmemStatic& S, const uin
     }
 }
 
+// The gate/up rows of one token at H = 2048 (P = 16 pairs, 64 chunks of 32 elements per
+// row): warp w takes pairs w and w + 8, lane l chunks l and l + 32 of each row, with
+// the lane's 64 x values read from shared memory once.  Per row the same sums as
+// gate_up_rows; the four per-lane row partials (gate and up of both pairs) meet in one
+// butterfly over the warp (6 shuffles instead of 4 x 5, the same additions in the same
+// order as a warp sum), after which lanes 0 and 16 hold gate and up of their pair.
+__device__ void gate_up_rows_t1_h2048(const DecodeArgs& a, const SmemStatic& S, const uint4* xs,
+                                      const uint8_t* wc, const uint8_t* ws, int tile, int pair0, int xr,
+                                      float s_gu) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int P = 16, rb = 1024, pieces = 256;
+    const int srow = 2048 / (a.mx ? 32 : 16);
+    uint4 xv[2][4];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+        for (int pi = 0; pi < 4; ++pi) xv[c2][pi] = xs[xr * pieces + xswz(4 * (lane + 32 * c2) + pi)];
+    float r[4];
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        const int p = warp + 8 * pp;
+        const uint8_t* cgp = wc + (size_t)p * rb;
+        const uint8_t* cup = wc + (size_t)(P + p) * rb;
+        const uint8_t* sgp = ws + (size_t)p * srow;
+        const uint8_t* sup = ws + (size_t)(P + p) * srow;
+        float ag = 0.f, au = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int ch = lane + 32 * c2;
+            const uint4 wg = *reinterpret_cast<const uint4*>(cgp + ch * 16);
+            const uint4 wu = *reinterpret_cast<const uint4*>(cup + ch * 16);
+            const float2 fg = chunk_scales(sgp, ch, a.mx);
+            const float2 fu = chunk_scales(sup, ch, a.mx);
+            const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
+            const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
+            float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f};
+#pragma unroll
+            for (int pi = 0; pi < 4; ++pi) {
+                uint32_t dg[4], du[4];
+                e2m1x8_to_f16x2(gw[pi], dg);
+                e2m1x8_to_f16x2(uw[pi], du);
+                pg[pi >> 1] = dot8_f16(dg, xv[c2][pi], pg[pi >> 1]);
+                pu[pi >> 1] = dot8_f16(du, xv[c2][pi], pu[pi >> 1]);
+            }
+            ag = fmaf(pg[0], fg.x, ag);
+            ag = fmaf(pg[1], fg.y, ag);
+            au = fmaf(pu[0], fu.x, au);
+            au = fmaf(pu[1], fu.y, au);
+        }
+        r[2 * pp] = ag;
+        r[2 * pp + 1] = au;
+    }
+    const bool b16 = (lane & 16) != 0, b8 = (lane & 8) != 0;
+    float a0 = b16 ? r[2] : r[0], a1 = b16 ? r[3] : r[1];
+    const float s0 = b16 ? r[0] : r[2], s1 = b16 ? r[1] : r[3];
+    a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    float c = b8 ? a1 : a0;
+    c += __shfl_xor_sync(0xffffffffu, b8 ? a0 : a1, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    const float up = __shfl_xor_sync(0xffffffffu, c, 8);
+    if ((lane & 15) == 0) {                               // lanes 0, 16: gate in c, up in `up`
+        const int p = warp + 8 * (lane >> 4);
+        const float xm = S.xmul[xr];
+        const float g = c * s_gu * xm;
+        const float uu = up * s_gu * xm;
+        const float hv = g / (1.f + expf(-g)) * uu;
+        st_relaxed_u64(a.h + (size_t)pair0 * a.I + tile * P + p, tagged(hv, S.tag));
+    }
+}
+
 // One gate/up item: every token group of the unit, on the staged weights.
 // (The caller has staged the item's weights with stage_gate_up.)
 __device__ void gate_up_item(const DecodeArgs& a, SmemStatic& S, uint4* xs, uint8_t* wc, uint8_t* ws,
@@ -696,7 +773,10 @@ __device__ void gate_up_item(const DecodeArgs& a, SmemStatic& S, uint4* xs, uint
         }
         __syncthreads();                                  // staged weights (fills) and x visible
         switch (ntg) {
-            case 1: gate_up_rows<1>(a, S, xs, wc, ws, tile, pair0 + g0, xrow, s_gu); break;
+            case 1:
+                if (a.H == 2048) gate_up_rows_t1_h2048(a, S, xs, wc, ws, tile, pair0 + g0, xrow[0], s_gu);
+                else gate_up_rows<1>(a, S, xs, wc, ws, tile, pair0 + g0, xrow, s_gu);
+                break;
             case 2: gate_up_rows<2>(a, S, xs, wc, ws, tile, pair0 + g0, xrow, s_gu); break;
             case 3: gate_up_rows<3>(a, S, xs, wc, ws, tile, pair0 + g0, xrow, s_gu); break;
             default: gate_up_rows<4>(a, S, xs, wc, ws, tile, pair0 + g0, xrow, s_gu); break;
@@ -835,6 +915,79 @@ __device__ void down_rows(const DecodeArgs& a, const SmemStatic& S, const float*
     }
 }
 
+// The down rows of one token at I = 512 (R = 64 rows per item, 16 chunks of 32 elements
+// per row): lane (sub, li) of warp w owns chunk li of rows w*8 + 2g + sub, g = 0..3.
+// The chunk's 32 h values are read into registers once; per row the chunk's partial
+// sums blocks as down_rows does; the four partials of a lane then meet across the 16
+// lanes of its half-warp in one butterfly (5 shuffles instead of 4 x 4), after which
+// lane li = 4g' of each half holds row 2g' + sub, and each pair of adjacent rows is
+// added into y with one vector add (two scalar adds when y is not 8-byte aligned).
+__device__ void down_rows_t1_i512(const DecodeArgs& a, const SmemStatic& S, const float* hs, const uint8_t* dc,
+                                  const uint8_t* ds, int rt, uint32_t tokmask, int g0, float s_d) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane >> 4, li = lane & 15;
+    const int srow = 512 / (a.mx ? 32 : 16);
+    const float4* hs4 = reinterpret_cast<const float4*>(hs);
+    float hv[32];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const float4 v = hs4[hswz(8 * li + p)];
+        hv[4 * p] = v.x;
+        hv[4 * p + 1] = v.y;
+        hv[4 * p + 2] = v.z;
+        hv[4 * p + 3] = v.w;
+    }
+    float res[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int rl = warp * 8 + 2 * g + sub;
+        const uint4 w4 = *reinterpret_cast<const uint4*>(dc + (size_t)rl * 256 + li * 16);
+        const float2 f = chunk_scales(ds + rl * srow, li, a.mx);
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int wq = 0; wq < 2; ++wq) {
+                uint32_t d[4];
+                e2m1x8_to_f16x2(ww[blk * 2 + wq], d);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&d[j]));
+                    const int e = blk * 16 + wq * 8 + 2 * j;
+                    p0 = fmaf(c2.x, hv[e], p0);
+                    p1 = fmaf(c2.y, hv[e + 1], p1);
+                }
+            }
+            acc = fmaf(p0 + p1, blk ? f.y : f.x, acc);
+        }
+        res[g] = acc;
+    }
+    const bool b8 = (li & 8) != 0, b4 = (li & 4) != 0;
+    float a0 = b8 ? res[2] : res[0], a1 = b8 ? res[3] : res[1];
+    const float s0 = b8 ? res[0] : res[2], s1 = b8 ? res[1] : res[3];
+    a0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+    a1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+    float c = b4 ? a1 : a0;
+    c += __shfl_xor_sync(0xffffffffu, b4 ? a0 : a1, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    const float c_odd = __shfl_xor_sync(0xffffffffu, c, 16);    // row 2g' + 1 (the other half)
+    if (sub == 0 && (li & 3) == 0) {
+        const int gq = 2 * (li >> 3) + ((li >> 2) & 1);
+        const int tok = (int)__fns(tokmask, 0, g0 + 1);
+        const float wsc = S.uw[g0] * s_d;
+        float* yp = a.y + (size_t)tok * a.H + rt * 64 + warp * 8 + 2 * gq;
+        if ((reinterpret_cast<uintptr_t>(yp) & 7) == 0) {
+            red_add_v2_f32(yp, wsc * c, wsc * c_odd);
+        } else {
+            red_add_f32(yp, wsc * c);
+            red_add_f32(yp + 1, wsc * c_odd);
+        }
+    }
+}
+
 // One down item: stage the weights (unless prefetched), wait for the unit's h,
 // then every token group, added into y.  A token's weight for a routed unit is the
 // sum of its routing weights to that expert (one route, unless the token lists the
@@ -885,7 +1038,10 @@ __device__ void down_item(const DecodeArgs& a, SmemStatic& S, const Decision& D,
         }
         __syncthreads();                                   // h (and the fills' weights) visible
         switch (ntg) {
-            case 1: down_rows<1>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
+            case 1:
+                if (I == 512) down_rows_t1_i512(a, S, hs, dc, ds, rt, tokmask, g0, s_d);
+                else down_rows<1>(a, S, hs, dc, ds, rt, tokmask, g0, s_d);
+                break;
             case 2: down_rows<2>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
             case 3: down_rows<3>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
             default: down_rows<4>(a, S, hs, dc, ds, rt, tokmask, g0, s_d); break;
