@@ -462,6 +462,20 @@ class DecodeRun:
             self.host.close()
 
 
+def busy_host_leg(ft, wlm, s, pool_ptr, shared, seed, rec_bytes, hbm_gbs, b_p, world, stream, n_threads):
+    """Full offload (the headline's split) with n_threads host workers spinning on their
+    cores and no branch attached: what idle host cores cost the host link's fills."""
+    spin = ft.HostBranch(s.L, s.E, s.H, s.I, s.k, s.B, pool_ptr, n_threads, mailbox=False)
+    try:
+        leg = decode_leg(ft, wlm, s, pool_ptr, shared, "full", 65536, seed, 32, 256, rec_bytes, hbm_gbs, b_p,
+                         world, stream)
+    finally:
+        spin.close()
+    leg["note"] = (f"{n_threads} host worker threads spinning on their cores during the run (nothing "
+                   "computed on the host); compare qwen_p0.8_full")
+    return leg
+
+
 def bandwidth_profile(ft, s, pool, shared, n_threads, n_records=64):
     """The two miss paths of this machine over n_records records of the pool: the GPU
     gather (fill path) and the host branch's GEMV, alone and together; the backend rule
@@ -632,6 +646,10 @@ def native(args, rank, world):
             legs[f"qwen_p{p}_qstar_hybrid"] = decode_leg(ft, wlm, sp, pool.ptr, shared, "qstar", f_half,
                                                          args.seed, 32, 256, rec_bytes, hbm_gbs, b_p,
                                                          world, stream, host_threads=n_host)
+        # the same full-offload decode while the host's cores are busy (the branch's
+        # workers spinning, nothing attached): the host link's fills depend on it
+        legs["qwen_p0.8_full_busy_host"] = busy_host_leg(ft, wlm, replace(s, p=0.8), pool.ptr, shared, args.seed,
+                                                         rec_bytes, hbm_gbs, b_p, world, stream, n_host)
         bw = bandwidth_profile(ft, s, pool, shared, n_host)
         out["bandwidth_profile"] = bw
         sp = replace(s, p=0.8)
