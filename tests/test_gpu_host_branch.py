@@ -40,18 +40,19 @@ def test_neon_host_share_matches_oracle(ft):
     hbt.test_host_share_qwen_shape(ft)
 
 
-@pytest.mark.parametrize("static", [False, True])
-def test_hybrid_decode_is_whole_layer(ft, wl_mod, static):
+@pytest.mark.parametrize("static,fmt", [(False, "nvfp4"), (True, "nvfp4"), (False, "mxfp4")])
+def test_hybrid_decode_is_whole_layer(ft, wl_mod, static, fmt):
     """q* split at f = 1/2 with a branch attached: tables bit-exact with the oracle,
     y = y_gpu + y_host against the oracle's full sum (shared expert included)."""
     L, E, H, I, k, B, C = 3, 16, 128, 64, 4, 2, 6
-    pool = wl_mod.build_pool(2, L, E, H, I)
-    shared = wl_mod.build_shared(2, L, H, I)
-    cache = ft.ExpertCache(L, E, H, I, k, B, C, pool.ptr, shared=shared, split=(ft.FT_SPLIT_QSTAR, 32768))
-    hb = ft.HostBranch(L, E, H, I, k, B, pool.ptr, 4)
+    pool = wl_mod.build_pool(2, L, E, H, I, fmt=fmt)
+    shared = wl_mod.build_shared(2, L, H, I, fmt=fmt)
+    cache = ft.ExpertCache(L, E, H, I, k, B, C, pool.ptr, shared=shared, split=(ft.FT_SPLIT_QSTAR, 32768),
+                           fmt=fmt)
+    hb = ft.HostBranch(L, E, H, I, k, B, pool.ptr, 4, fmt=fmt)
     ft.ft_cache_set_host_branch(cache.handle, hb.handle)
     ref = SlotCache(L, E, C, full_offload=False, f_q16=32768)
-    experts = oracle_experts(2, H, I)
+    experts = oracle_experts(2, H, I, fmt)
     rng = np.random.default_rng(11)
     x = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
     y = torch.empty((B, H), dtype=torch.float32, device="cuda")
@@ -71,7 +72,7 @@ def test_hybrid_decode_is_whole_layer(ft, wl_mod, static):
         assert ct.cpu().numpy().tolist() == [r.n_hit, r.m, r.q, r.n_def_routes]
         n_host_calls += r.n_def_routes > 0
         xx = x.float().cpu().numpy()
-        y_ref = decode_layer(xx, ids, gates, l, E, experts, oracle_shared(2, l, H, I))
+        y_ref = decode_layer(xx, ids, gates, l, E, experts, oracle_shared(2, l, H, I, fmt))
         assert_close(y.cpu().numpy(), y_ref, f"call {call}")
     assert n_host_calls > 5
     jobs, mailbox_jobs = ft.ft_host_branch_stats(hb.handle)
