@@ -3,6 +3,7 @@ from __future__ import annotations
 
 import glob
 import os
+import platform
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
 
@@ -15,6 +16,9 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxe
 # host-only sources (the CPU branch): the host C++ compiler, no contraction of a*b+c
 # into fused operations beyond the ones the code writes out
 CXXFLAGS = ["-O3", "-std=c++17", "-fPIC", "-pthread", "-ffp-contract=off"]
+if platform.machine() == "aarch64":
+    # the host GEMV's f16 widening multiply-add (FMLAL); Grace (Neoverse V2) has it
+    CXXFLAGS += ["-march=armv8.2-a+fp16+fp16fml"]
 
 
 def _nvcc() -> str:

@@ -11,15 +11,16 @@
 // [BWRATIO "代码全链路" §2] the host side receives -1 for every route the GPU
 //   keeps, and the two partials are added.
 //
-// Arithmetic (the same on every host): x (bf16) is taken exactly as fp32; each E2M1
-// code is read as twice its value (a small integer, exact) and the factor 1/2 rides on
-// its block scale (E4M3, or E8M0 for MXFP4 records, as fp32); a row is a sum over
-// 16-element groups: lane j of a group accumulates elements j, 4+j, 8+j, 12+j with
-// fused multiply-adds, the group partial is (l0 + l1) + (l2 + l3) and enters the row
-// sum through one fused multiply-add with the group's scale.  The NEON path
-// (aarch64) and the portable path perform exactly these operations in this order.
-// Then g, u = row * s_gu, h = silu(g) * u, o = (W_d h) * s_d, y[b] += w * o with the
-// units in ascending flat id.
+// Arithmetic (the same on every host): x (bf16) is rounded to f16 after a per-token
+// power-of-two prescale that keeps |x| < 2^15 (exact for bf16 values in the f16 normal
+// range); E2M1 codes and block scales (E4M3, or E8M0 for MXFP4 records) are exact in
+// f16 / fp32; a row is a sum over 16-element groups: lane j of a group accumulates
+// elements j, 4+j, 8+j, 12+j with fused multiply-adds of exact products starting from
+// zero, the group partial is (l0 + l1) + (l2 + l3) and enters the row sum through one
+// fused multiply-add with the group's scale.  On aarch64 the gate/up rows use the f16
+// widening multiply-add (FMLAL) and the down rows fp32 NEON; elsewhere the same
+// operations run one element at a time.  Then g, u = row * s_gu * prescale,
+// h = silu(g) * u, o = (W_d h) * s_d, y[b] += w * o with the units in ascending flat id.
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -36,6 +37,9 @@
 #if defined(__aarch64__)
 #include <arm_neon.h>
 #endif
+#if defined(__aarch64__) && defined(__ARM_FEATURE_FP16_FML)
+#define FT_HOST_FMLAL 1
+#endif
 
 #include "../../include/ft.h"
 #include "ft_host.h"
@@ -44,22 +48,26 @@
 namespace ft {
 namespace {
 
-// Twice the value of each E2M1 code (sign in bit 3).
-alignas(16) constexpr int8_t kE2M1x2[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+// The value of each E2M1 code (sign in bit 3), and the high byte of its f16 encoding
+// (every E2M1 value has a zero low byte in f16).
+constexpr float kE2M1[16] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f,
+                             -0.f, -0.5f, -1.f, -1.5f, -2.f, -3.f, -4.f, -6.f};
+alignas(16) constexpr uint8_t kE2M1f16hi[16] = {0x00, 0x38, 0x3C, 0x3E, 0x40, 0x42, 0x44, 0x46,
+                                                0x80, 0xB8, 0xBC, 0xBE, 0xC0, 0xC2, 0xC4, 0xC6};
 
-// Half the value of each E4M3 code (sign bit 7, exponent bits 6..3 with bias 7,
-// mantissa bits 2..0; exponent 0 is subnormal; 0x7F / 0xFF are NaN) and of each E8M0
-// code (2^(c - 127); 0xFF is NaN).
+// The value of each E4M3 code (sign bit 7, exponent bits 6..3 with bias 7, mantissa
+// bits 2..0; exponent 0 is subnormal; 0x7F / 0xFF are NaN) and of each E8M0 code
+// (2^(c - 127); 0xFF is NaN).
 struct ScaleTables {
-    float e4m3_half[256];
-    float e8m0_half[256];
+    float e4m3[256];
+    float e8m0[256];
     ScaleTables() {
         for (int c = 0; c < 256; ++c) {
             const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
             float v = e == 0 ? std::ldexp((float)m / 8.f, -6) : std::ldexp(1.f + (float)m / 8.f, e - 7);
             if ((c & 127) == 127) v = NAN;
-            e4m3_half[c] = (s ? -v : v) * 0.5f;
-            e8m0_half[c] = c == 255 ? NAN : std::ldexp(1.f, c - 128);
+            e4m3[c] = s ? -v : v;
+            e8m0[c] = c == 255 ? NAN : std::ldexp(1.f, c - 127);
         }
     }
 };
@@ -68,30 +76,68 @@ const ScaleTables& tables() {
     return t;
 }
 
-// out[t] = sum over the K elements of one staged row of code * v[t][k] * scale, for
-// NT vectors (the arithmetic of the file comment).
+// f16 encoding of a float, round to nearest even (the sign kept; values past the f16
+// range become infinity, values below half the smallest subnormal zero).
+uint16_t f16_bits(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const uint32_t a = u & 0x7FFFFFFFu;
+    if (a >= 0x7F800000u) return (uint16_t)(sign | 0x7C00u | (a > 0x7F800000u ? 0x200u : 0u));
+    const int e = (int)(a >> 23) - 127;                       // unbiased exponent
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);
+    uint32_t mant, base;
+    int shift;                                                 // low bits dropped
+    if (e >= -14) {                                            // normal: 10 of 23 bits kept
+        mant = a & 0x7FFFFFu;
+        base = (uint32_t)(e + 15) << 10;
+        shift = 13;
+    } else {                                                   // subnormal: units of 2^-24
+        mant = (a & 0x7FFFFFu) | 0x800000u;
+        base = 0;
+        shift = -e - 1;
+        if (shift > 24) return (uint16_t)sign;
+    }
+    const uint32_t q = mant >> shift;
+    const uint32_t rem = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    uint32_t r = base + q;
+    if (rem > half || (rem == half && (q & 1u))) r += 1;       // a carry moves into the exponent
+    return (uint16_t)(sign | r);
+}
+
+float f16_value(uint16_t h) {
+    const uint32_t e = (h >> 10) & 31, m = h & 1023;
+    float v = e == 0 ? std::ldexp((float)m, -24) : std::ldexp((float)(m | 1024), (int)e - 25);
+    if (e == 31) v = m ? NAN : INFINITY;
+    return (h & 0x8000) ? -v : v;
+}
+
+inline float group_sum(const float* a) { return (a[0] + a[1]) + (a[2] + a[3]); }
+
+// out[t] = sum over the K elements of one row of code * v[t][k] * scale, for NT
+// vectors of fp32 values (the down rows; also the gate/up rows where FMLAL is absent).
 template <int NT>
 void row_dot(const uint8_t* codes, const uint8_t* scales, int K, bool mx, const float* const* v, float* out) {
-    const float* sct = mx ? tables().e8m0_half : tables().e4m3_half;
+    const float* sct = mx ? tables().e8m0 : tables().e4m3;
     float row[NT];
     for (int t = 0; t < NT; ++t) row[t] = 0.f;
     const int ng = K / 16;
 #if defined(__aarch64__)
-    const int8x16_t tab = vld1q_s8(kE2M1x2);
+    const uint8x16_t tab = vld1q_u8(kE2M1f16hi);
     const uint8x8_t m15 = vdup_n_u8(15);
+    const uint8x16_t zero = vdupq_n_u8(0);
     for (int gi = 0; gi < ng; ++gi) {
         const float sc = sct[scales[mx ? gi >> 1 : gi]];
         const uint8x8_t b = vld1_u8(codes + 8 * gi);
         const uint8x8x2_t z = vzip_u8(vand_u8(b, m15), vshr_n_u8(b, 4));
-        const int8x16_t c8 = vqtbl1q_s8(tab, vcombine_u8(z.val[0], z.val[1]));
-        const int16x8_t c16a = vmovl_s8(vget_low_s8(c8)), c16b = vmovl_high_s8(c8);
-        const float32x4_t c0 = vcvtq_f32_s32(vmovl_s16(vget_low_s16(c16a)));
-        const float32x4_t c1 = vcvtq_f32_s32(vmovl_high_s16(c16a));
-        const float32x4_t c2 = vcvtq_f32_s32(vmovl_s16(vget_low_s16(c16b)));
-        const float32x4_t c3 = vcvtq_f32_s32(vmovl_high_s16(c16b));
+        const uint8x16_t hi = vqtbl1q_u8(tab, vcombine_u8(z.val[0], z.val[1]));
+        const float16x8_t h0 = vreinterpretq_f16_u8(vzip1q_u8(zero, hi));
+        const float16x8_t h1 = vreinterpretq_f16_u8(vzip2q_u8(zero, hi));
+        const float32x4_t c0 = vcvt_f32_f16(vget_low_f16(h0)), c1 = vcvt_high_f32_f16(h0);
+        const float32x4_t c2 = vcvt_f32_f16(vget_low_f16(h1)), c3 = vcvt_high_f32_f16(h1);
         for (int t = 0; t < NT; ++t) {
             const float* xv = v[t] + 16 * gi;
-            float32x4_t a = vmulq_f32(c0, vld1q_f32(xv));
+            float32x4_t a = vfmaq_f32(vdupq_n_f32(0.f), c0, vld1q_f32(xv));
             a = vfmaq_f32(a, c1, vld1q_f32(xv + 4));
             a = vfmaq_f32(a, c2, vld1q_f32(xv + 8));
             a = vfmaq_f32(a, c3, vld1q_f32(xv + 12));
@@ -105,21 +151,55 @@ void row_dot(const uint8_t* codes, const uint8_t* scales, int K, bool mx, const 
         float c[16];
         for (int i = 0; i < 8; ++i) {
             const uint8_t b = codes[8 * gi + i];
-            c[2 * i] = (float)kE2M1x2[b & 15];
-            c[2 * i + 1] = (float)kE2M1x2[b >> 4];
+            c[2 * i] = kE2M1[b & 15];
+            c[2 * i + 1] = kE2M1[b >> 4];
         }
         for (int t = 0; t < NT; ++t) {
             const float* xv = v[t] + 16 * gi;
-            float a[4];
-            for (int j = 0; j < 4; ++j) a[j] = c[j] * xv[j];
-            for (int q = 1; q < 4; ++q)
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < 4; ++q)
                 for (int j = 0; j < 4; ++j) a[j] = std::fma(c[4 * q + j], xv[4 * q + j], a[j]);
-            row[t] = std::fma((a[0] + a[1]) + (a[2] + a[3]), sc, row[t]);
+            row[t] = std::fma(group_sum(a), sc, row[t]);
         }
     }
 #endif
     for (int t = 0; t < NT; ++t) out[t] = row[t];
 }
+
+#if defined(FT_HOST_FMLAL)
+// The same sums for NT vectors of f16 values (the gate/up rows): FMLAL multiplies f16
+// pairs exactly and adds them into fp32 lanes with one rounding, in the lane order
+// above.
+template <int NT>
+void row_dot_h(const uint8_t* codes, const uint8_t* scales, int K, bool mx, const uint16_t* const* v, float* out) {
+    const float* sct = mx ? tables().e8m0 : tables().e4m3;
+    float row[NT];
+    for (int t = 0; t < NT; ++t) row[t] = 0.f;
+    const int ng = K / 16;
+    const uint8x16_t tab = vld1q_u8(kE2M1f16hi);
+    const uint8x8_t m15 = vdup_n_u8(15);
+    const uint8x16_t zero = vdupq_n_u8(0);
+    for (int gi = 0; gi < ng; ++gi) {
+        const float sc = sct[scales[mx ? gi >> 1 : gi]];
+        const uint8x8_t b = vld1_u8(codes + 8 * gi);
+        const uint8x8x2_t z = vzip_u8(vand_u8(b, m15), vshr_n_u8(b, 4));
+        const uint8x16_t hi = vqtbl1q_u8(tab, vcombine_u8(z.val[0], z.val[1]));
+        const float16x8_t h0 = vreinterpretq_f16_u8(vzip1q_u8(zero, hi));
+        const float16x8_t h1 = vreinterpretq_f16_u8(vzip2q_u8(zero, hi));
+        for (int t = 0; t < NT; ++t) {
+            const float16x8_t x0 = vreinterpretq_f16_u16(vld1q_u16(v[t] + 16 * gi));
+            const float16x8_t x1 = vreinterpretq_f16_u16(vld1q_u16(v[t] + 16 * gi + 8));
+            float32x4_t a = vfmlalq_low_f16(vdupq_n_f32(0.f), h0, x0);
+            a = vfmlalq_high_f16(a, h0, x0);
+            a = vfmlalq_low_f16(a, h1, x1);
+            a = vfmlalq_high_f16(a, h1, x1);
+            const float32x2_t s2 = vpadd_f32(vget_low_f32(a), vget_high_f32(a));
+            row[t] = std::fma(vget_lane_f32(s2, 0) + vget_lane_f32(s2, 1), sc, row[t]);
+        }
+    }
+    for (int t = 0; t < NT; ++t) out[t] = row[t];
+}
+#endif
 
 // Any number of vectors, in groups of up to four.
 void row_dot_n(const uint8_t* codes, const uint8_t* scales, int K, bool mx, const float* const* v, int n,
@@ -132,6 +212,25 @@ void row_dot_n(const uint8_t* codes, const uint8_t* scales, int K, bool mx, cons
             default: row_dot<4>(codes, scales, K, mx, v + t0, out + t0); break;
         }
     }
+}
+
+// The gate/up rows: x as f16 (vh) or as the fp32 values of the same f16 numbers (vf).
+void row_dot_x(const uint8_t* codes, const uint8_t* scales, int K, bool mx, const uint16_t* const* vh,
+               const float* const* vf, int n, float* out) {
+#if defined(FT_HOST_FMLAL)
+    (void)vf;
+    for (int t0 = 0; t0 < n; t0 += 4) {
+        switch (std::min(4, n - t0)) {
+            case 1: row_dot_h<1>(codes, scales, K, mx, vh + t0, out + t0); break;
+            case 2: row_dot_h<2>(codes, scales, K, mx, vh + t0, out + t0); break;
+            case 3: row_dot_h<3>(codes, scales, K, mx, vh + t0, out + t0); break;
+            default: row_dot_h<4>(codes, scales, K, mx, vh + t0, out + t0); break;
+        }
+    }
+#else
+    (void)vh;
+    row_dot_n(codes, scales, K, mx, vf, n, out);
+#endif
 }
 
 inline float bf16_to_float(uint16_t b) {
@@ -173,7 +272,9 @@ struct ft_host_branch {
     std::vector<ft::Unit> units;
     int n_pairs = 0;
     int B = 0;
-    std::vector<float> xf;     // [B_max, H]
+    std::vector<float> xf;     // [B_max, H] x / xmul rounded to f16, as fp32
+    std::vector<uint16_t> xh;  // the same numbers as f16
+    float xmul[32];            // per-token power-of-two prescale
     std::vector<float> h;      // [pairs, I]
     float* y = nullptr;        // [B, H]
     int n1 = 0, n2 = 0;
@@ -192,15 +293,20 @@ struct ft_host_branch {
         float s_gu;
         std::memcpy(&s_gu, rec + rl.s_gu, 4);
         const float* xv[32];
-        for (int t = 0; t < u.ntok; ++t) xv[t] = xf.data() + (size_t)u.tok[t] * H;
+        const uint16_t* xhv[32];
+        for (int t = 0; t < u.ntok; ++t) {
+            xv[t] = xf.data() + (size_t)u.tok[t] * H;
+            xhv[t] = xh.data() + (size_t)u.tok[t] * H;
+        }
         float g[32], uu[32];
         for (int p = p0; p < p0 + ft::kChunk; ++p) {
-            ft::row_dot_n(rec + rl.gu_codes + (size_t)p * (H / 2), rec + rl.gu_scales + (size_t)p * (H / sb), H,
-                          mx, xv, u.ntok, g);
-            ft::row_dot_n(rec + rl.gu_codes + (size_t)(I + p) * (H / 2),
-                          rec + rl.gu_scales + (size_t)(I + p) * (H / sb), H, mx, xv, u.ntok, uu);
+            ft::row_dot_x(rec + rl.gu_codes + (size_t)p * (H / 2), rec + rl.gu_scales + (size_t)p * (H / sb), H,
+                          mx, xhv, xv, u.ntok, g);
+            ft::row_dot_x(rec + rl.gu_codes + (size_t)(I + p) * (H / 2),
+                          rec + rl.gu_scales + (size_t)(I + p) * (H / sb), H, mx, xhv, xv, u.ntok, uu);
             for (int t = 0; t < u.ntok; ++t) {
-                const float gv = g[t] * s_gu, uv = uu[t] * s_gu;
+                const float xm = xmul[u.tok[t]];
+                const float gv = g[t] * s_gu * xm, uv = uu[t] * s_gu * xm;
                 h[(size_t)(u.pair0 + t) * I + p] = gv / (1.f + std::exp(-gv)) * uv;
             }
         }
@@ -284,8 +390,20 @@ struct ft_host_branch {
             std::this_thread::yield();
         jobs.fetch_add(1, std::memory_order_relaxed);
     }
+    // x of the job's tokens: per token a power of two 2^k (k = 0 unless |x| reaches 2^15)
+    // and x / 2^k rounded to f16.
     void load_x(const uint16_t* x, int B_) {
-        for (size_t i = 0; i < (size_t)B_ * H; ++i) xf[i] = ft::bf16_to_float(x[i]);
+        for (int b = 0; b < B_; ++b) {
+            float amax = 0.f;
+            for (int i = 0; i < H; ++i) amax = std::max(amax, std::fabs(ft::bf16_to_float(x[(size_t)b * H + i])));
+            const int k = amax >= 32768.f ? std::ilogb(amax) - 14 : 0;
+            xmul[b] = std::ldexp(1.f, k);
+            for (int i = 0; i < H; ++i) {
+                const size_t j = (size_t)b * H + i;
+                xh[j] = ft::f16_bits(std::ldexp(ft::bf16_to_float(x[j]), -k));
+                xf[j] = ft::f16_value(xh[j]);
+            }
+        }
     }
     ft::MailboxHeader* header() { return reinterpret_cast<ft::MailboxHeader*>(mailbox); }
     // A call published by the decode kernel: compute it into the mailbox's y, then
@@ -372,7 +490,7 @@ double host_branch_run_flats(ft_host_branch* hb, const int32_t* flats, int n) {
     std::vector<int32_t> def(flats, flats + n);
     std::vector<float> w(n, 1.f);
     std::vector<float> y((size_t)hb->H);
-    std::vector<uint16_t> x((size_t)hb->H, 0x3c00);   // bf16 1.0
+    std::vector<uint16_t> x((size_t)hb->H, 0x3F80);   // bf16 1.0
     const auto t0 = std::chrono::steady_clock::now();
     hb->B = 1;
     hb->y = y.data();
@@ -427,6 +545,7 @@ ft_status ft_host_branch_create(const ft_host_desc* d, ft_host_branch** out) {
     hb->nthreads = d->n_threads;
     hb->cpus = cpus;
     hb->xf.resize((size_t)d->B_max * d->H);
+    hb->xh.resize((size_t)d->B_max * d->H);
     hb->h.resize((size_t)(d->B_max * d->k_max) * d->I);
     if (hb->mailbox) {
         ft::MailboxHeader* hd = hb->header();

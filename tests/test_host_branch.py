@@ -150,3 +150,19 @@ def test_recommend_and_overlap_split_match_the_library(ft):
         assert ft.ft_recommend_backend(cpu, pcie) == want
         assert ft.ft_split_from_overlap(pcie, cpu) == split_from_overlap(pcie, cpu)
     assert ft.ft_recommend_backend(100.0, 50.0) == ft.FT_BACKEND_OFFLOAD
+
+
+def test_host_share_large_activations(ft):
+    """x scaled by 2^20 (beyond the f16 range): the per-token power-of-two prescale keeps
+    the f16 copy of x exact, so the partial still matches the oracle in fp32 accuracy."""
+    L, E, H, I, k, B, layer, seed = 1, 8, 64, 32, 2, 2, 0, 4
+    pool = _pool(seed, L, E, H, I)
+    x = synth.decode_x(seed, 0, 0, L, B, H, "cpu").float().numpy() * np.float32(2.0 ** 20)
+    ids = np.array([[1, 5], [5, 2]], np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5]], np.float32)
+    deferred = ids.astype(np.int32).copy()
+    y = _host_partial(ft, pool, L, E, H, I, x, deferred, w, B, k, 2)
+    with np.errstate(over="ignore"):                     # silu of large negative g: e^-g -> inf, silu -> 0
+        y_ref = decode_layer(x, ids, w, layer, E, oracle_experts(seed, H, I), include=deferred >= 0)
+    rel = np.linalg.norm(y - y_ref) / np.linalg.norm(y_ref)
+    assert rel < 1e-5, rel
