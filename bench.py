@@ -858,9 +858,10 @@ def native_prefill(args, ft, wlm, pool, b_p, world):
 
 def prefill_on_demand_leg(args, ft, wlm, pool, b_p, world, xs, routes, y, capacity=200):
     """The same chunk with fewer slots than one layer's experts: every layer falls back
-    to loading its routed union on demand, in groups of at most `capacity` experts
-    (the gathers cannot overlap the group's GEMMs).  Bound: the records it fills over
-    the host link at B_P."""
+    to loading its routed union on demand, in groups of at most `capacity` experts,
+    each gathered in batches whose GEMMs run beside the next batch's gather (a group
+    cannot overlap the previous group's GEMMs: its victims are their slots).  Bound:
+    the records it fills over the host link at B_P."""
     import torch
     s = wlm.SHAPES[args.prefill_workload]
     T, L = s.T, s.L
@@ -911,7 +912,8 @@ def prefill_on_demand_leg(args, ft, wlm, pool, b_p, world, xs, routes, y, capaci
             "gather_gbs": streamed / (g_ms / 1e3) / 1e9 if g_ms else None,
             "gemm1_ms_per_layer": prof["prefill_gemm1"][0] / L, "gemm2_ms_per_layer": prof["prefill_gemm2"][0] / L,
             "note": "chunk from an emptied cache each time; DOUBLE_BUFFER asked for, 200 < 2E slots: "
-                    "on-demand fallback; gathers and GEMMs of a group run one after the other"}
+                    "on-demand fallback; a group's records are gathered in batches, each batch's GEMMs "
+                    "beside the next batch's gather; groups follow one another"}
 
 
 def prefill_mx_leg(args, ft, wlm, world):

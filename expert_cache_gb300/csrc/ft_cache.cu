@@ -51,6 +51,7 @@ WsLayout ws_layout(const ft_cache_desc& d) {
         w.pf_fill_flat = take((size_t)d.E * 4);
         w.pf_fill_slot = take((size_t)d.E * 4);
         w.pf_nfill = take(4);
+        w.pf_sub = take((size_t)2 * (ft::kOdSub + 1) * 4);
     }
     w.total = off;
     return w;
@@ -256,6 +257,7 @@ ft_status ft_cache_create(const ft_cache_desc* d, ft_cache** out) {
         cudaEventCreateWithFlags(&c->compute_done[i], cudaEventDisableTiming);
     }
     cudaEventCreateWithFlags(&c->entry_ev, cudaEventDisableTiming);
+    for (int i = 0; i <= kOdSub; ++i) cudaEventCreateWithFlags(&c->od_ev[i], cudaEventDisableTiming);
     c->maps_ok = prefill_maps(c);
     uint8_t* ws = c->workspace;
     e = launch_init_tables(reinterpret_cast<int32_t*>(ws + c->ws.slot_for_id), d->L * d->E,
@@ -282,6 +284,7 @@ void ft_cache_destroy(ft_cache* c) {
         cudaEventDestroy(c->compute_done[i]);
     }
     cudaEventDestroy(c->entry_ev);
+    for (int i = 0; i <= kOdSub; ++i) cudaEventDestroy(c->od_ev[i]);
     if (c->prof_n >= 0) {
         for (int i = 0; i < ft_cache::kProfEvents; ++i)
             if (c->prof_ev[i]) cudaEventDestroy(c->prof_ev[i]);
@@ -586,10 +589,10 @@ ft_status ft_profile_bandwidth(ft_cache* c, ft_host_branch* hb, int32_t n, void*
     e = cudaMemcpy(dv, lists.data(), lists.size() * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaEventCreate(&ev[0]);
     if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
-    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, s);          // warm-up
+    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, false, s);          // warm-up
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = cudaEventRecord(ev[0], s);
-    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, s);
+    if (e == cudaSuccess) e = ft::launch_pf_gather(ga, false, s);
     if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
     if (e == cudaSuccess) e = cudaEventSynchronize(ev[1]);
     if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
@@ -604,7 +607,7 @@ ft_status ft_profile_bandwidth(ft_cache* c, ft_host_branch* hb, int32_t n, void*
     if (e == cudaSuccess) {
         reps = (int)std::max(1.0, std::min(64.0, std::round(t_c / std::max(t_p, 1e-9))));
         e = cudaEventRecord(ev[0], s);
-        for (int r = 0; r < reps && e == cudaSuccess; ++r) e = ft::launch_pf_gather(ga, s);
+        for (int r = 0; r < reps && e == cudaSuccess; ++r) e = ft::launch_pf_gather(ga, false, s);
         if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
     }
     if (e == cudaSuccess) {

@@ -33,6 +33,7 @@ constexpr int kExpertsPerThread = kMaxE / kThreadsRemap;   // 4
 // Decode layer kernel tiling.
 constexpr int kDecThreads = 256;       // 8 warps
 constexpr int kTokGroup = 4;           // tokens accumulated per pass
+constexpr int kOdSub = 8;              // on-demand prefill: gather / GEMM batches per group
 
 // Work items of the decode kernel: a gate/up item holds decode_pairs(H) (gate row,
 // up row) pairs and a down item decode_rows(I) output rows, each at most 32 KB of
@@ -74,7 +75,7 @@ struct WsLayout {
     size_t pf_chunk_cnt, pf_offsets, pf_mtile, pf_perm, pf_route_pos;
     size_t pf_a_codes, pf_a_scales, pf_h_codes, pf_h_scales, pf_o;
     // on-demand prefill: per-group expert -> slot, tile prefix and fill list
-    size_t pf_slot_of, pf_gmtile, pf_fill_flat, pf_fill_slot, pf_nfill;
+    size_t pf_slot_of, pf_gmtile, pf_fill_flat, pf_fill_slot, pf_nfill, pf_sub;
     size_t total;
 };
 
@@ -225,6 +226,7 @@ struct ft_cache {
     int buffer_layer[2];            // layer last streamed into each prefill buffer (-1 none)
     bool copy_pending;
     cudaEvent_t entry_ev;           // work enqueued before a prefill call
+    cudaEvent_t od_ev[ft::kOdSub + 1];  // on-demand prefill: group tables done, batches gathered
     CUtensorMap map_a1, map_b1;     // GEMM1: quantised x rows; W_gu codes of the slots
     CUtensorMap map_a2, map_b2;     // GEMM2: quantised h rows; W_d codes of the slots
     bool maps_ok;

@@ -13,7 +13,12 @@
 // every miss filled, in groups of at most C experts in ascending id; per group the
 // table kernel picks the victims, a gather kernel streams the missing records from
 // the pinned pool into them over the host link, and the two GEMMs run on the group's
-// rows before the next group may evict them.
+// rows before the next group may evict them.  A group is gathered in kOdSub batches
+// on the copy stream (one CTA on half of the SMs), and the GEMMs of batch j run on
+// the caller's stream as soon as its records are in, beside the gather of batch j+1:
+// a batch's victims are slots no other expert of the group uses, so the batches need
+// no other order.  (8 batches per group measured best against 2, 4 and 16, and half of
+// the SMs for the gathers against a quarter and all.)
 //
 // Streams: the caller's stream computes; the cache's copy stream moves whole layers
 // (E contiguous records of the pool into E contiguous slots: one streaming kernel of
@@ -173,6 +178,7 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
     g.I = d.I; g.H = d.H;
     g.slot0 = b * d.E;
     g.slot_of = nullptr;
+    g.mrange = nullptr;
     g.mx = d.format == FT_FORMAT_MXFP4 ? 1 : 0;
     g.slot_buf = c->slot_buf;
     g.rec_bytes = rec;
@@ -228,6 +234,8 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
         da.fill_flat = reinterpret_cast<int32_t*>(ws + c->ws.pf_fill_flat);
         da.fill_slot = reinterpret_cast<int32_t*>(ws + c->ws.pf_fill_slot);
         da.n_fill = reinterpret_cast<int32_t*>(ws + c->ws.pf_nfill);
+        da.sub_fill = reinterpret_cast<int32_t*>(ws + c->ws.pf_sub);
+        da.sub_tile = da.sub_fill + (kOdSub + 1);
         PrefillGatherArgs ga;
         ga.host_pool = c->host_pool_dev;
         ga.slot_buf = c->slot_buf;
@@ -235,17 +243,41 @@ extern "C" ft_status ft_moe_prefill_layer(ft_cache* c, int32_t layer, const void
         ga.fill_flat = da.fill_flat;
         ga.fill_slot = da.fill_slot;
         ga.n_fill = da.n_fill;
+        ga.sub_fill = da.sub_fill;
         g.slot_of = da.slot_of;
         g.mtile_prefix = da.mtile;
+        // a batch's gather on the copy stream, timed there when copies are profiled
+        auto gather = [&](int j) -> cudaError_t {
+            cudaEvent_t e1 = nullptr;
+            if ((c->prof & (1u << 4)) && c->prof_n * 2 + 2 <= ft_cache::kProfEvents) {
+                const int i = c->prof_n++;
+                c->prof_kind[i] = 4;
+                cudaEventRecord(c->prof_ev[2 * i], c->copy_stream);
+                e1 = c->prof_ev[2 * i + 1];
+            }
+            ga.sub = j;
+            const cudaError_t r = launch_pf_gather(ga, true, c->copy_stream);
+            if (e1) cudaEventRecord(e1, c->copy_stream);
+            return r;
+        };
         const int groups = (d.E + c->C - 1) / c->C;
         for (int grp = 0; grp < groups; ++grp) {
             da.group = grp;
             if (prof_kernel(3, [&] { return launch_pf_demand_tables(da, s); }) != cudaSuccess)
                 return fail(FT_ERR_CUDA, "on-demand table launch");
-            if (prof_kernel(4, [&] { return launch_pf_gather(ga, s); }) != cudaSuccess)
-                return fail(FT_ERR_CUDA, "on-demand gather launch");
-            const ft_status st = gemms();
-            if (st != FT_OK) return st;
+            cudaEventRecord(c->od_ev[kOdSub], s);
+            cudaStreamWaitEvent(c->copy_stream, c->od_ev[kOdSub], 0);
+            for (int j = 0; j < kOdSub; ++j) {
+                if (gather(j) != cudaSuccess) return fail(FT_ERR_CUDA, "on-demand gather launch");
+                cudaEventRecord(c->od_ev[j], c->copy_stream);
+            }
+            for (int j = 0; j < kOdSub; ++j) {
+                cudaStreamWaitEvent(s, c->od_ev[j], 0);
+                g.mrange = da.sub_tile + j;
+                const ft_status st = gemms();
+                if (st != FT_OK) return st;
+            }
+            g.mrange = nullptr;
         }
     }
 

@@ -51,6 +51,10 @@ struct PrefillDemandArgs {
     int32_t* fill_flat;         // [E] out: flat id of fill i (ascending)
     int32_t* fill_slot;         // [E] out: victim slot of fill i
     int32_t* n_fill;            // out: number of fills
+    // out: the group in kOdSub batches by expert id, each starting at a fill: batch j
+    // holds fills [sub_fill[j], sub_fill[j+1]) and 128-row tiles [sub_tile[j], sub_tile[j+1])
+    int32_t* sub_fill;          // [kOdSub + 1]
+    int32_t* sub_tile;          // [kOdSub + 1]
 };
 
 struct PrefillGatherArgs {
@@ -60,6 +64,8 @@ struct PrefillGatherArgs {
     const int32_t* fill_flat;
     const int32_t* fill_slot;
     const int32_t* n_fill;
+    const int32_t* sub_fill;    // when not null: fills [sub_fill[sub], sub_fill[sub + 1]) only
+    int sub;
 };
 
 cudaError_t launch_pf_tables(const PrefillTablesArgs& a, cudaStream_t s);
@@ -67,7 +73,8 @@ cudaError_t launch_pf_tables(const PrefillTablesArgs& a, cudaStream_t s);
 // host memory) to dst (device).
 cudaError_t launch_pf_stream(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_pf_demand_tables(const PrefillDemandArgs& a, cudaStream_t s);
-cudaError_t launch_pf_gather(const PrefillGatherArgs& a, cudaStream_t s);
+// narrow: half of the SMs (one CTA each), beside the GEMMs of the previous batch
+cudaError_t launch_pf_gather(const PrefillGatherArgs& a, bool narrow, cudaStream_t s);
 cudaError_t launch_pf_sort_quant(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_pf_combine(const PrefillArgs& a, cudaStream_t s);
 

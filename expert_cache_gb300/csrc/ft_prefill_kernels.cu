@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(1024, 1) pf_demand_tables_kernel(PrefillDemand
             *a.n_fill = 0;
             if (a.group == 0) a.sc->tick = a.sc->tick + 1;   // the call still ticks once
         }
+        if (tid <= kOdSub) { a.sub_fill[tid] = 0; a.sub_tile[tid] = 0; }
         return;
     }
     int m = 0;
@@ -203,6 +204,18 @@ __global__ void __launch_bounds__(1024, 1) pf_demand_tables_kernel(PrefillDemand
         }
     }
     if (tid == 0) { a.mtile[E] = all_tiles; *a.n_fill = m; }
+    __syncthreads();                               // mtile and fill_flat complete
+    // ---- batches: batch j starts at fill j*m/kOdSub and at the first tile of that
+    // fill's expert (fills run in ascending expert id), so its tiles are those of the
+    // members from that expert up to the next batch's; batch 0 starts at tile 0
+    if (tid <= kOdSub) {
+        const int f = (int)((long long)tid * m / kOdSub);
+        int t = all_tiles;
+        if (tid == 0) t = 0;
+        else if (f < m) t = a.mtile[a.fill_flat[f] - a.layer * E];
+        a.sub_fill[tid] = f;
+        a.sub_tile[tid] = t;
+    }
     // ---- LRU order: untouched slots keep their order, touched ones follow ascending
     int n_untouched = 0;
 #pragma unroll
@@ -229,27 +242,30 @@ __global__ void __launch_bounds__(1024, 1) pf_demand_tables_kernel(PrefillDemand
     if (tid == 0) a.sc->tick = tick;
 }
 
-// Fill records of one on-demand group: pinned pool -> victim slots, 16-byte pieces
-// read over the host link by every thread of the grid, four in flight per thread.
-__global__ void pf_gather_kernel(PrefillGatherArgs a) {
-    const int n = *a.n_fill;
+// Fill records of one on-demand group (or of one of its batches): pinned pool ->
+// victim slots, 16-byte pieces read over the host link by every thread of the grid,
+// eight in flight per thread.
+__global__ void __launch_bounds__(256) pf_gather_kernel(PrefillGatherArgs a) {
+    const int f0 = a.sub_fill ? a.sub_fill[a.sub] : 0;
+    const int f1 = a.sub_fill ? a.sub_fill[a.sub + 1] : *a.n_fill;
+    if (f1 <= f0) return;
     const size_t per = a.rec_bytes / 16;
-    const size_t total = (size_t)n * per;
-    const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
-    for (size_t i0 = (size_t)blockIdx.x * blockDim.x * 4 + threadIdx.x; i0 < total; i0 += stride) {
-        uint4 v[4];
-        size_t dst[4];
+    const size_t total = (size_t)(f1 - f0) * per;
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 8;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x * 8 + threadIdx.x; i0 < total; i0 += stride) {
+        uint4 v[8];
+        size_t dst[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
             const size_t i = i0 + (size_t)j * blockDim.x;
             if (i < total) {
-                const size_t r = i / per, off = (i % per) * 16;
-                v[j] = *reinterpret_cast<const uint4*>(a.host_pool + (size_t)a.fill_flat[r] * a.rec_bytes + off);
+                const size_t r = f0 + i / per, off = (i % per) * 16;
+                v[j] = __ldcs(reinterpret_cast<const uint4*>(a.host_pool + (size_t)a.fill_flat[r] * a.rec_bytes + off));
                 dst[j] = (size_t)a.fill_slot[r] * a.rec_bytes + off;
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
             const size_t i = i0 + (size_t)j * blockDim.x;
             if (i < total) *reinterpret_cast<uint4*>(a.slot_buf + dst[j]) = v[j];
         }
@@ -443,8 +459,9 @@ cudaError_t launch_pf_demand_tables(const PrefillDemandArgs& a, cudaStream_t s) 
     return cudaGetLastError();
 }
 
-cudaError_t launch_pf_gather(const PrefillGatherArgs& a, cudaStream_t s) {
-    pf_gather_kernel<<<sm_count() * 4, 256, 0, s>>>(a);
+cudaError_t launch_pf_gather(const PrefillGatherArgs& a, bool narrow, cudaStream_t s) {
+    const int half = sm_count() / 2;
+    pf_gather_kernel<<<narrow ? (half > 0 ? half : 1) : sm_count() * 4, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

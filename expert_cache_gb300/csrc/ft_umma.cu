@@ -158,7 +158,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total = g.mtile_prefix[g.E] * g.n_tiles_n;
+    // tiles of m-tiles [m_lo, m_hi) (all of them unless a range is given), n fastest
+    const int m_lo = g.mrange ? g.mrange[0] : 0;
+    const int m_hi = g.mrange ? g.mrange[1] : g.mtile_prefix[g.E];
+    const int total = max(m_hi - m_lo, 0) * g.n_tiles_n;
+    const int tile0 = m_lo * g.n_tiles_n;
     const int kstages = g.K / 256;
 
     if (threadIdx.x == 0) {
@@ -187,7 +191,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         bool ok = true;
         int scale_bad = 0;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const TileInfo ti = tile_info(g, tile);
+            const TileInfo ti = tile_info(g, tile0 + tile);
             const int slot = g.slot_of ? g.slot_of[ti.e] : g.slot0 + ti.e;
             const uint8_t* rec = g.slot_buf + (size_t)slot * g.rec_bytes;
             for (int ks = 0; ks < kstages; ++ks, ++it) {
@@ -325,7 +329,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         int tl = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tl) {
-            const TileInfo ti = tile_info(g, tile);
+            const TileInfo ti = tile_info(g, tile0 + tile);
             if (!mbar_wait(&acc_full, (uint32_t)tl & 1u, &abort_flag)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const bool valid = r < ti.rows;

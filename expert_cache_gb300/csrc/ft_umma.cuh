@@ -21,6 +21,7 @@ struct UmmaArgs {
     const uint8_t* a_scales;    // [R_max, K/16]
     const int32_t* offsets;     // [E + 1]
     const int32_t* mtile_prefix;// [E + 1]
+    const int32_t* mrange;      // when not null: only m-tiles [mrange[0], mrange[1])
     const int32_t* perm;        // sorted row -> route
     const float* w;             // gates by route
     uint8_t* h_codes;           // kind 1 outputs (sorted rows)

@@ -199,8 +199,9 @@ ft_status ft_moe_decode_static(ft_cache* c, int32_t layer, const void* x,
  * valid route, ascending id) goes through the global LRU like decode misses with every
  * miss filled, in groups of at most C experts (one tick per group, the first group
  * ticks even for an empty union); each group's missing records are streamed from the
- * pinned pool into their victim slots by the GPU and the group is computed before the
- * next one may evict it.  What is resident afterwards is decode's cache.  Activations and h are NVFP4 (unit
+ * pinned pool into their victim slots by the GPU (in batches on the cache's copy
+ * stream, each batch computed beside the next one's stream-in) and the group is
+ * computed before the next one may evict it.  What is resident afterwards is decode's cache.  Activations and h are NVFP4 (unit
  * tensor scale, E4M3 per 16); the two grouped GEMMs run on tcgen05 block-scaled
  * FP4 tensor cores; y[t] = sum_j w[t,j] * o_(t,j) in order j.
  *   x         device bf16 [T, H];  topk_ids device int32 [T, k];  topk_w device fp32 [T, k]
