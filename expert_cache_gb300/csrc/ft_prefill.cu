@@ -24,7 +24,8 @@
 // (E contiguous records of the pool into E contiguous slots: one streaming kernel of
 // SM loads from the device-mapped pool per layer.  On some boxes a copy-engine
 // transfer issued on this stream ran at 72-90 GB/s while copies on another stream ran
-// at 211 GB/s; SM loads do not depend on the copy engine a stream is given).
+// at 211 GB/s; SM loads do not depend on the copy engine a stream is given), and the
+// on-demand batches.
 //   copy(l+1 -> buffer b')  waits for everything enqueued before this call (the
 //                            previous layer, the last reader of b');
 //   compute(l)              waits for copy(l -> b).
